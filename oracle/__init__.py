@@ -1,0 +1,186 @@
+"""fp64 CPU oracle of the Mamba2 mixer core (conv + SiLU, softplus dt,
+selective-SSM recurrence; sequential, chunked and one-step forms).
+
+TEST INFRASTRUCTURE. Only tests/, the smoke check in __graft_entry__.py and
+the cpu_baseline / reference leg of bench.py may import this package. The
+CUDA library (full_duplex_speech_gb300) never imports it, and it never
+imports the CUDA library: the two share no code. Inputs reach both from the
+seeded_inputs module, which holds none of the mixer's arithmetic.
+
+The arithmetic lives in mamba2_oracle.c (plain C, fp64, optional OpenMP over
+(batch, head) units). This module compiles it with gcc, loads it with
+ctypes, and converts numpy arrays to fp64 on the way in.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+from seeded_inputs import Dims, as_f64
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mamba2_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libm2oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class _Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("batch", "T", "H", "P", "N", "G", "K")]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into oracle/_build/libm2oracle.so (gcc, -O2, no
+    fast-math: IEEE fp64 semantics are kept)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.c_int
+            lib.m2o_softplus.restype = ctypes.c_double
+            lib.m2o_softplus.argtypes = [ctypes.c_double]
+            lib.m2o_silu.restype = ctypes.c_double
+            lib.m2o_silu.argtypes = [ctypes.c_double]
+            lib.m2o_max_threads.restype = ip
+            lib.m2o_ssm.argtypes = [ctypes.POINTER(_Dims)] + [dp] * 8 + [ip] * 4
+            lib.m2o_conv_silu.argtypes = [ctypes.POINTER(_Dims)] + [dp] * 7 + [ip]
+            lib.m2o_conv_tail.argtypes = [ctypes.POINTER(_Dims)] + [dp] * 5
+            lib.m2o_mixer_scan.argtypes = [ctypes.POINTER(_Dims)] + [dp] * 14 + [ip] * 4
+            lib.m2o_mixer_step.argtypes = [ctypes.POINTER(_Dims), ip] + [dp] * 12 + [ip]
+            for f in ("m2o_ssm", "m2o_conv_silu", "m2o_conv_tail", "m2o_mixer_scan", "m2o_mixer_step"):
+                getattr(lib, f).restype = ip
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _dims(d: Dims, batch: int, T: int) -> _Dims:
+    return _Dims(batch, T, d.H, d.P, d.N, d.G, d.K)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise RuntimeError(f"oracle {what} failed with status {rc}")
+
+
+def max_threads() -> int:
+    return int(_load().m2o_max_threads())
+
+
+def softplus(z: float) -> float:
+    return float(_load().m2o_softplus(float(z)))
+
+
+def silu(u: float) -> float:
+    return float(_load().m2o_silu(float(u)))
+
+
+def conv_silu(d: Dims, x, B, C, conv_w, conv_b, init_conv=None, nthreads: int = 0) -> np.ndarray:
+    """Post-conv, post-SiLU activations [b,T,CH] from fp64 pre-conv inputs."""
+    x, B, C = _f64(x), _f64(B), _f64(C)
+    b, T = x.shape[0], x.shape[1]
+    out = np.empty((b, T, d.CH), dtype=np.float64)
+    ic = None if init_conv is None else _f64(init_conv)
+    rc = _load().m2o_conv_silu(ctypes.byref(_dims(d, b, T)), _ptr(x), _ptr(B), _ptr(C),
+                               _ptr(_f64(conv_w)), _ptr(_f64(conv_b)), _ptr(ic), _ptr(out), nthreads)
+    _check(rc, "conv_silu")
+    return out
+
+
+def conv_tail(d: Dims, x, B, C, init_conv=None) -> np.ndarray:
+    """The last K-1 pre-conv frames [b,K-1,CH] (oldest first)."""
+    x, B, C = _f64(x), _f64(B), _f64(C)
+    b, T = x.shape[0], x.shape[1]
+    out = np.empty((b, d.K - 1, d.CH), dtype=np.float64)
+    ic = None if init_conv is None else _f64(init_conv)
+    rc = _load().m2o_conv_tail(ctypes.byref(_dims(d, b, T)), _ptr(x), _ptr(B), _ptr(C), _ptr(ic), _ptr(out))
+    _check(rc, "conv_tail")
+    return out
+
+
+def ssm(d: Dims, xt, Bt, Ct, dt, A, D, h0=None, chunk: int = 0, heads=None, nthreads: int = 0):
+    """SSM core on post-conv inputs. xt [b,T,H,P], Bt/Ct [b,T,G,N], dt [b,T,H]
+    (after softplus), A, D [H]. chunk <= 0: sequential; else chunked with
+    that chunk length. Returns (y [b,T,H,P], h [b,H,P,N])."""
+    xt, Bt, Ct, dt = _f64(xt), _f64(Bt), _f64(Ct), _f64(dt)
+    b, T = xt.shape[0], xt.shape[1]
+    lo, hi = (0, d.H) if heads is None else heads
+    h = np.zeros((b, d.H, d.P, d.N)) if h0 is None else _f64(h0).copy()
+    y = np.zeros((b, T, d.H, d.P))
+    rc = _load().m2o_ssm(ctypes.byref(_dims(d, b, T)), _ptr(xt), _ptr(Bt), _ptr(Ct), _ptr(dt),
+                         _ptr(_f64(A)), _ptr(_f64(D)), _ptr(h), _ptr(y), lo, hi, chunk, nthreads)
+    _check(rc, "ssm")
+    return y, h
+
+
+def mixer_scan(d: Dims, inp: dict, init_ssm=None, init_conv=None, chunk: int = 0, heads=None,
+               nthreads: int = 0):
+    """Whole mixer core over a sequence from seeded_inputs-style arrays
+    (bf16 bits or fp32 activations, fp32 parameters).
+
+    Returns dict(y [b,T,H,P] fp64, final_ssm [b,H,P,N] fp64,
+    final_conv [b,K-1,CH] fp64). With heads=(lo, hi) only those heads of y
+    and final_ssm are computed (the rest stay zero)."""
+    act = inp["act"]
+    x, B, C, dtr = (as_f64(inp[k], act) for k in ("x", "B", "C", "dt_raw"))
+    b, T = x.shape[0], x.shape[1]
+    lo, hi = (0, d.H) if heads is None else heads
+    ic = None if init_conv is None else as_f64(init_conv, act)
+    iss = None if init_ssm is None else _f64(init_ssm)
+    y = np.zeros((b, T, d.H, d.P))
+    fs = np.zeros((b, d.H, d.P, d.N))
+    fc = np.zeros((b, d.K - 1, d.CH))
+    rc = _load().m2o_mixer_scan(
+        ctypes.byref(_dims(d, b, T)), _ptr(x), _ptr(B), _ptr(C), _ptr(dtr),
+        _ptr(_f64(inp["A_log"])), _ptr(_f64(inp["D"])), _ptr(_f64(inp["dt_bias"])),
+        _ptr(_f64(inp["conv_w"])), _ptr(_f64(inp["conv_b"])), _ptr(iss), _ptr(ic),
+        _ptr(y), _ptr(fs), _ptr(fc), lo, hi, chunk, nthreads)
+    _check(rc, "mixer_scan")
+    return dict(y=y, final_ssm=fs, final_conv=fc)
+
+
+def mixer_step(d: Dims, frame: dict, params: dict, ssm_state, conv_state, nthreads: int = 0):
+    """One cached frame for S sessions. frame holds x [S,H,P], B/C [S,G,N],
+    dt_raw [S,H] (bf16 bits or fp32, with 'act'); ssm_state [S,H,P,N] and
+    conv_state [S,K-1,CH] are fp64 arrays updated in place. Returns y [S,H,P]."""
+    act = frame["act"]
+    x, B, C, dtr = (as_f64(frame[k], act) for k in ("x", "B", "C", "dt_raw"))
+    S = x.shape[0]
+    assert ssm_state.dtype == np.float64 and ssm_state.flags.c_contiguous
+    assert conv_state.dtype == np.float64 and conv_state.flags.c_contiguous
+    y = np.zeros((S, d.H, d.P))
+    rc = _load().m2o_mixer_step(
+        ctypes.byref(_dims(d, 1, 1)), S, _ptr(x), _ptr(B), _ptr(C), _ptr(dtr),
+        _ptr(_f64(params["A_log"])), _ptr(_f64(params["D"])), _ptr(_f64(params["dt_bias"])),
+        _ptr(_f64(params["conv_w"])), _ptr(_f64(params["conv_b"])), _ptr(ssm_state),
+        _ptr(conv_state), _ptr(y), nthreads)
+    _check(rc, "mixer_step")
+    return y

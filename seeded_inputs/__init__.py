@@ -1,0 +1,181 @@
+"""Seeded synthetic inputs for the Mamba2 mixer core, shared by the oracle's
+tests, the CUDA parity tests and bench.py.
+
+This module draws random numbers and converts between storage formats. It
+holds none of the mixer's arithmetic (no conv, SiLU, softplus, exp or scan):
+that lives, independently, in the oracle and in the CUDA library.
+
+Shapes and distributions follow the Nemotron-H text_config of the VoiceChat
+checkpoint (issue "feat(nemotron_voicechat): load the VoiceChat checkpoint and
+run offline duplex inference", section config.json / text_config:
+mamba_num_heads 128, mamba_head_dim 80, ssm_state_size 128, n_groups 8,
+conv_kernel 4, use_conv_bias true). No checkpoint or dataset is involved; the
+activations and weights are drawn from these distributions:
+
+  x, B, C (pre-conv)  ~ N(0, 1)
+  dt_raw              ~ N(0, 0.5)            (sigma 0.5)
+  dt_bias             = inverse softplus of a log-uniform draw in [1e-3, 0.1]
+  A_log               = log U[1, 16]
+  D                   ~ N(0, 1)
+  conv_w, conv_b      ~ U(-0.5, 0.5)          (conv weight stored [CH, K])
+
+Activations are stored as bf16 (as uint16 bit patterns, round-to-nearest-even
+from fp32) or as fp32; parameters are fp32.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+__all__ = [
+    "Dims",
+    "REAL_SHAPE",
+    "TINY_SHAPE",
+    "MAMBA_LAYERS",
+    "mixer_params",
+    "mixer_activations",
+    "mixer_inputs",
+    "f32_to_bf16_bits",
+    "f64_to_bf16_bits",
+    "bf16_bits_to_f64",
+    "bf16_bits_to_f32",
+    "as_f64",
+    "conv_state_inputs",
+    "ssm_state_inputs",
+]
+
+
+@dataclass(frozen=True)
+class Dims:
+    """Mixer dimensions. CH = H*P + 2*G*N conv channels (x | B | C)."""
+
+    H: int  # mamba_num_heads
+    P: int  # mamba_head_dim
+    N: int  # ssm_state_size
+    G: int  # n_groups
+    K: int = 4  # conv_kernel
+
+    @property
+    def CH(self) -> int:
+        return self.H * self.P + 2 * self.G * self.N
+
+    @property
+    def R(self) -> int:
+        """Heads per group."""
+        return self.H // self.G
+
+
+# Nemotron-H mixer shape from the VoiceChat text_config.
+REAL_SHAPE = Dims(H=128, P=80, N=128, G=8, K=4)
+# The tiny fp32 mixer used for brute-force checks: 4 heads x 16, state 16, 1 group.
+TINY_SHAPE = Dims(H=4, P=16, N=16, G=1, K=4)
+
+# Layer indices of the Mamba ('M') entries of hybrid_override_pattern
+# "M-M-M-MM-M-M-M*-M-M-M*-M-M-M-M*-M-M-M-M*-M-MM-M-M-M-M-M-" (27 of 56 layers).
+_PATTERN = "M-M-M-MM-M-M-M*-M-M-M*-M-M-M-M*-M-M-M-M*-M-MM-M-M-M-M-M-"
+MAMBA_LAYERS = tuple(i for i, ch in enumerate(_PATTERN) if ch == "M")
+
+
+# ---------------------------------------------------------------- bf16 codec
+def f32_to_bf16_bits(a) -> np.ndarray:
+    """fp32 -> bf16 bit patterns (uint16), round to nearest, ties to even.
+    Inputs are finite (no NaN handling needed for these distributions)."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
+
+
+def f64_to_bf16_bits(a) -> np.ndarray:
+    """fp64 -> bf16 bit patterns with a single round-to-nearest-even step
+    (no double rounding through fp32). Valid for finite values in the
+    normal bf16 range and for exact zeros; values below 2**-126 in magnitude
+    are flushed to signed zero."""
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    bits = a.view(np.uint64)
+    sign = (bits >> np.uint64(63)).astype(np.uint64)
+    mag = bits & np.uint64(0x7FFFFFFFFFFFFFFF)
+    # bf16 keeps 7 explicit mantissa bits; fp64 has 52 -> drop 45 bits.
+    drop = np.uint64(45)
+    half = np.uint64(1) << (drop - np.uint64(1))
+    lsb = (mag >> drop) & np.uint64(1)
+    rounded = (mag + half - np.uint64(1) + lsb) >> drop << drop
+    r64 = rounded.view(np.float64)
+    tiny = r64 < 2.0 ** -126
+    r32 = r64.astype(np.float32)  # exact: at most 8 significant bits
+    out = (r32.view(np.uint32) >> 16).astype(np.uint16)
+    out = np.where(tiny, np.uint16(0), out)
+    out = out | (sign.astype(np.uint16) << np.uint16(15))
+    return out.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b) -> np.ndarray:
+    """bf16 bit patterns -> fp32 (exact)."""
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def bf16_bits_to_f64(b) -> np.ndarray:
+    """bf16 bit patterns -> fp64 (exact)."""
+    return bf16_bits_to_f32(b).astype(np.float64)
+
+
+# ---------------------------------------------------------------- generators
+def mixer_params(seed: int, d: Dims) -> dict:
+    """Per-layer parameters (fp32): A_log, D, dt_bias [H]; conv_w [CH, K];
+    conv_b [CH]."""
+    rng = np.random.default_rng([seed, 0x5EED, 1])
+    dt_target = np.exp(rng.uniform(np.log(1e-3), np.log(0.1), size=d.H))
+    # inverse softplus of the target step size: the draw is specified as such
+    dt_bias = np.log(np.expm1(dt_target))
+    A_log = np.log(rng.uniform(1.0, 16.0, size=d.H))
+    D = rng.standard_normal(d.H)
+    conv_w = rng.uniform(-0.5, 0.5, size=(d.CH, d.K))
+    conv_b = rng.uniform(-0.5, 0.5, size=d.CH)
+    f = lambda v: np.ascontiguousarray(v, dtype=np.float32)  # noqa: E731
+    return dict(A_log=f(A_log), D=f(D), dt_bias=f(dt_bias), conv_w=f(conv_w), conv_b=f(conv_b))
+
+
+def mixer_activations(seed: int, d: Dims, batch: int, T: int, act: str = "bf16") -> dict:
+    """Pre-conv activations x [b,T,H,P], B [b,T,G,N], C [b,T,G,N],
+    dt_raw [b,T,H]. act='bf16' -> uint16 bit patterns; act='f32' -> float32."""
+    rng = np.random.default_rng([seed, 0x5EED, 2])
+    x = rng.standard_normal((batch, T, d.H, d.P), dtype=np.float32)
+    B = rng.standard_normal((batch, T, d.G, d.N), dtype=np.float32)
+    C = rng.standard_normal((batch, T, d.G, d.N), dtype=np.float32)
+    dt_raw = (0.5 * rng.standard_normal((batch, T, d.H), dtype=np.float32)).astype(np.float32)
+    out = dict(x=x, B=B, C=C, dt_raw=dt_raw)
+    if act == "bf16":
+        out = {k: f32_to_bf16_bits(v) for k, v in out.items()}
+    elif act != "f32":
+        raise ValueError(f"act must be 'bf16' or 'f32', got {act!r}")
+    return out
+
+
+def mixer_inputs(seed: int, d: Dims, batch: int, T: int, act: str = "bf16") -> dict:
+    """Parameters and activations of one mixer layer, both from `seed`."""
+    p = mixer_params(seed, d)
+    p.update(mixer_activations(seed, d, batch, T, act))
+    p["act"] = act
+    return p
+
+
+def as_f64(a, act: str) -> np.ndarray:
+    """Exact fp64 view of a stored activation (bf16 bits or fp32)."""
+    if act == "bf16":
+        return bf16_bits_to_f64(a)
+    return np.asarray(a, dtype=np.float32).astype(np.float64)
+
+
+def conv_state_inputs(seed: int, d: Dims, batch: int, act: str = "bf16") -> np.ndarray:
+    """A random pre-conv conv tail [b, K-1, CH] (x|B|C channel order), used as
+    an initial conv state in continuation tests."""
+    rng = np.random.default_rng([seed, 0x5EED, 3])
+    v = rng.standard_normal((batch, d.K - 1, d.CH), dtype=np.float32)
+    return f32_to_bf16_bits(v) if act == "bf16" else v
+
+
+def ssm_state_inputs(seed: int, d: Dims, batch: int, scale: float = 0.05) -> np.ndarray:
+    """A random fp32 SSM state [b, H, P, N] for continuation tests."""
+    rng = np.random.default_rng([seed, 0x5EED, 4])
+    return (scale * rng.standard_normal((batch, d.H, d.P, d.N))).astype(np.float32)
