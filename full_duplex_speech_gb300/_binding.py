@@ -1,0 +1,143 @@
+"""ctypes binding of libmamba2.so: the same names as the C ABI, argument
+marshalling only. Tensor arguments may be torch tensors (their data_ptr()
+is passed), plain ints (device addresses) or None (NULL)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libmamba2.so")
+_lock = threading.Lock()
+_lib = None
+
+BF16 = 0
+F32 = 1
+
+STATUS = {0: "M2_OK", 1: "M2_EINVAL", 2: "M2_ESHAPE", 3: "M2_EALIGN", 4: "M2_EUNSUPPORTED",
+          5: "M2_ECUDA", 6: "M2_EWORKSPACE"}
+
+
+class M2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {STATUS.get(status, status)} ({mamba2_status_string(status)})"
+        if status == 5:
+            msg += f", cudaError {mamba2_last_cuda_error()}"
+        super().__init__(msg)
+
+
+class M2Dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("T", ctypes.c_int), ("nheads", ctypes.c_int),
+                ("headdim", ctypes.c_int), ("dstate", ctypes.c_int), ("ngroups", ctypes.c_int),
+                ("dconv", ctypes.c_int), ("act", ctypes.c_int)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libmamba2.so (built by full_duplex_speech_gb300.build). Raises
+    if it is missing: there is no other implementation to fall back to."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libmamba2.so not found at {_LIB_PATH}; run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, sz, ip = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        dp = ctypes.POINTER(M2Dims)
+        lib.mamba2_scan_workspace_bytes.argtypes = [dp, ip]
+        lib.mamba2_scan_workspace_bytes.restype = sz
+        lib.mamba2_conv_scan.argtypes = [dp] + [vp] * 9 + [ip] + [vp] * 6 + [sz, vp]
+        lib.mamba2_conv_scan.restype = ip
+        lib.mamba2_step_workspace_bytes.argtypes = [dp, ip]
+        lib.mamba2_step_workspace_bytes.restype = sz
+        lib.mamba2_step.argtypes = [dp, ip] + [vp] * 13 + [sz, vp]
+        lib.mamba2_step.restype = ip
+        lib.mamba2_status_string.argtypes = [ip]
+        lib.mamba2_status_string.restype = ctypes.c_char_p
+        lib.mamba2_last_cuda_error.argtypes = []
+        lib.mamba2_last_cuda_error.restype = ip
+        lib.mamba2_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+        lib.mamba2_device_error.restype = ip
+        _lib = lib
+        return lib
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def dims(batch, T, H, P, N, G, K=4, act=BF16) -> M2Dims:
+    if isinstance(act, str):
+        act = {"bf16": BF16, "f32": F32}[act]
+    return M2Dims(batch, T, H, P, N, G, K, act)
+
+
+def mamba2_status_string(status: int) -> str:
+    return load().mamba2_status_string(status).decode()
+
+
+def mamba2_last_cuda_error() -> int:
+    return load().mamba2_last_cuda_error()
+
+
+def mamba2_device_error(stream=None) -> int:
+    code = ctypes.c_uint(0)
+    rc = load().mamba2_device_error(_stream(stream), ctypes.byref(code))
+    if rc:
+        raise M2Error(rc, "mamba2_device_error")
+    return code.value
+
+
+def mamba2_scan_workspace_bytes(d: M2Dims, chunk: int) -> int:
+    return load().mamba2_scan_workspace_bytes(ctypes.byref(d), chunk)
+
+
+def mamba2_step_workspace_bytes(d: M2Dims, n_sessions: int) -> int:
+    return load().mamba2_step_workspace_bytes(ctypes.byref(d), n_sessions)
+
+
+def mamba2_conv_scan(d: M2Dims, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk,
+                     init_ssm, init_conv, y, final_ssm, final_conv, workspace, workspace_bytes=None,
+                     stream=None, check=True) -> int:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().mamba2_conv_scan(
+        ctypes.byref(d), _p(x), _p(B), _p(C), _p(dt_raw), _p(A_log), _p(D), _p(dt_bias), _p(conv_w),
+        _p(conv_b), int(chunk), _p(init_ssm), _p(init_conv), _p(y), _p(final_ssm), _p(final_conv),
+        _p(workspace), int(workspace_bytes), _stream(stream))
+    if check and rc:
+        raise M2Error(rc, "mamba2_conv_scan")
+    return rc
+
+
+def mamba2_step(d: M2Dims, n_sessions, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, ssm_state,
+                conv_state, y, workspace, workspace_bytes=None, stream=None, check=True) -> int:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().mamba2_step(
+        ctypes.byref(d), int(n_sessions), _p(x), _p(B), _p(C), _p(dt_raw), _p(A_log), _p(D),
+        _p(dt_bias), _p(conv_w), _p(conv_b), _p(ssm_state), _p(conv_state), _p(y), _p(workspace),
+        int(workspace_bytes), _stream(stream))
+    if check and rc:
+        raise M2Error(rc, "mamba2_step")
+    return rc

@@ -1,0 +1,216 @@
+// The C ABI of libmamba2.so (declared in include/mamba2.h): argument,
+// shape and alignment validation on the host, then dispatch to the kernel
+// launchers. Nothing here allocates device memory.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mamba2.h"
+#include "m2_launch.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+// Device error word: bounded waits inside the kernels record why they gave up.
+__device__ unsigned int g_dev_error = 0;
+
+constexpr int kMaxDevices = 64;
+// Per-device facts resolved once: 0 = unknown, 1 = sm_103, 2 = other.
+int g_dev_kind[kMaxDevices] = {0};
+unsigned int* g_dev_error_ptr[kMaxDevices] = {nullptr};
+
+m2_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return M2_ECUDA;
+}
+
+m2_status current_device(int* dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (*dev < 0 || *dev >= kMaxDevices) return M2_EUNSUPPORTED;
+    if (g_dev_kind[*dev] == 0) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dev_error);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_dev_error_ptr[*dev] = static_cast<unsigned int*>(p);
+        g_dev_kind[*dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return g_dev_kind[*dev] == 1 ? M2_OK : M2_EUNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+m2_status check_dims(const m2_dims* d, bool need_seq) {
+    if (!d) return M2_EINVAL;
+    if (d->nheads <= 0 || d->headdim <= 0 || d->dstate <= 0 || d->ngroups <= 0 || d->dconv <= 0)
+        return M2_EINVAL;
+    if (need_seq && (d->batch < 0 || d->T < 0)) return M2_EINVAL;
+    if (d->act != M2_BF16 && d->act != M2_F32) return M2_EINVAL;
+    if (d->dconv != 4) return M2_ESHAPE;
+    const int N = d->dstate;
+    if (N != 16 && N != 32 && N != 64 && N != 128) return M2_ESHAPE;
+    if (d->headdim % 16 != 0 || d->headdim > 96) return M2_ESHAPE;
+    if (d->nheads % d->ngroups != 0) return M2_ESHAPE;
+    if (((long)d->nheads * d->headdim) % 8 != 0 || ((long)d->ngroups * N) % 8 != 0) return M2_ESHAPE;
+    return M2_OK;
+}
+
+m2::Shape shape_of(const m2_dims* d) {
+    m2::Shape s;
+    s.H = d->nheads;
+    s.P = d->headdim;
+    s.N = d->dstate;
+    s.G = d->ngroups;
+    s.K = d->dconv;
+    s.bf16 = d->act == M2_BF16;
+    return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mamba2_status_string(m2_status s) {
+    switch (s) {
+        case M2_OK: return "ok";
+        case M2_EINVAL: return "invalid argument (null pointer or non-positive size)";
+        case M2_ESHAPE: return "unsupported dimensions";
+        case M2_EALIGN: return "pointer not 16-byte aligned";
+        case M2_EUNSUPPORTED: return "current device is not an sm_103 GPU";
+        case M2_ECUDA: return "CUDA error (see mamba2_last_cuda_error)";
+        case M2_EWORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+int mamba2_last_cuda_error(void) { return g_last_cuda_error; }
+
+m2_status mamba2_device_error(void* stream, unsigned int* code) {
+    if (!code) return M2_EINVAL;
+    int dev = 0;
+    m2_status st = current_device(&dev);
+    if (st != M2_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyAsync(code, g_dev_error_ptr[dev], sizeof(unsigned int),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(g_dev_error_ptr[dev], &zero, sizeof(unsigned int), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return e == cudaSuccess ? M2_OK : cuda_fail(e);
+}
+
+size_t mamba2_step_workspace_bytes(const m2_dims* d, int n_sessions) {
+    if (check_dims(d, false) != M2_OK || n_sessions < 0) return 0;
+    return m2::step_workspace_bytes(shape_of(d), n_sessions);
+}
+
+m2_status mamba2_step(const m2_dims* d, int n_sessions, const void* x, const void* B,
+                      const void* C, const void* dt_raw, const float* A_log, const float* D,
+                      const float* dt_bias, const float* conv_w, const float* conv_b,
+                      float* ssm_state, void* conv_state, void* y, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    m2_status st = check_dims(d, false);
+    if (st != M2_OK) return st;
+    if (n_sessions < 0) return M2_EINVAL;
+    const void* ptrs[] = {x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, ssm_state, conv_state, y};
+    for (const void* p : ptrs)
+        if (!p) return M2_EINVAL;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return M2_EALIGN;
+    const m2::Shape s = shape_of(d);
+    const size_t need = m2::step_workspace_bytes(s, n_sessions);
+    if (!workspace || workspace_bytes < need) return M2_EWORKSPACE;
+    if (!aligned16(workspace)) return M2_EALIGN;
+    int dev = 0;
+    st = current_device(&dev);
+    if (st != M2_OK) return st;
+    if (n_sessions == 0) return M2_OK;
+
+    m2::StepArgs a;
+    a.s = s;
+    a.S = n_sessions;
+    a.x = x;
+    a.B = B;
+    a.C = C;
+    a.dt_raw = dt_raw;
+    a.A_log = A_log;
+    a.D = D;
+    a.dt_bias = dt_bias;
+    a.conv_w = conv_w;
+    a.conv_b = conv_b;
+    a.ssm = ssm_state;
+    a.conv = conv_state;
+    a.y = y;
+    a.ws_u = static_cast<float*>(workspace);
+    a.ws_dt = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       ((size_t)n_sessions * s.CH() * 4 + 255) / 256 * 256);
+    cudaError_t e = m2::launch_step(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M2_OK : cuda_fail(e);
+}
+
+size_t mamba2_scan_workspace_bytes(const m2_dims* d, int chunk) {
+    if (check_dims(d, true) != M2_OK || chunk < 1 || chunk > 128) return 0;
+    return m2::scan_workspace_bytes(shape_of(d), d->batch, d->T, chunk);
+}
+
+m2_status mamba2_conv_scan(const m2_dims* d, const void* x, const void* B, const void* C,
+                           const void* dt_raw, const float* A_log, const float* D,
+                           const float* dt_bias, const float* conv_w, const float* conv_b,
+                           int chunk, const float* init_ssm, const void* init_conv, void* y,
+                           float* final_ssm, void* final_conv, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    m2_status st = check_dims(d, true);
+    if (st != M2_OK) return st;
+    if (chunk < 1 || chunk > 128) return M2_EINVAL;
+    const void* ptrs[] = {x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, y, final_ssm, final_conv};
+    const bool empty = d->batch == 0 || d->T == 0;
+    for (int i = 0; i < 12; ++i) {
+        // sequence inputs and y may be NULL when there are no frames
+        const bool seq = (i < 4) || i == 9;
+        if (!ptrs[i] && !(empty && seq)) return M2_EINVAL;
+    }
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return M2_EALIGN;
+    if ((init_ssm && !aligned16(init_ssm)) || (init_conv && !aligned16(init_conv))) return M2_EALIGN;
+    const m2::Shape s = shape_of(d);
+    const size_t need = m2::scan_workspace_bytes(s, d->batch, d->T, chunk);
+    if (need && (!workspace || workspace_bytes < need)) return M2_EWORKSPACE;
+    if (workspace && !aligned16(workspace)) return M2_EALIGN;
+    int dev = 0;
+    st = current_device(&dev);
+    if (st != M2_OK) return st;
+    if (d->batch == 0) return M2_OK;
+
+    m2::ScanArgs a;
+    a.s = s;
+    a.batch = d->batch;
+    a.T = d->T;
+    a.chunk = chunk;
+    a.x = x;
+    a.B = B;
+    a.C = C;
+    a.dt_raw = dt_raw;
+    a.A_log = A_log;
+    a.D = D;
+    a.dt_bias = dt_bias;
+    a.conv_w = conv_w;
+    a.conv_b = conv_b;
+    a.init_ssm = init_ssm;
+    a.init_conv = init_conv;
+    a.y = y;
+    a.final_ssm = final_ssm;
+    a.final_conv = final_conv;
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
+    a.err = g_dev_error_ptr[dev];
+    cudaError_t e = m2::launch_scan(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M2_OK : cuda_fail(e);
+}
+
+}  // extern "C"

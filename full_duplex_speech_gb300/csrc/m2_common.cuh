@@ -1,0 +1,93 @@
+// Shared device helpers of the Mamba2 mixer-core kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace m2 {
+
+// Activation element types: bf16 travels as its 16-bit pattern.
+struct bf16_t { uint16_t bits; };
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// 8 consecutive activations -> fp32 (16 B of bf16 or 32 B of fp32).
+template <typename TA> struct Act8;
+
+template <> struct Act8<bf16_t> {
+    uint4 raw;
+    __device__ __forceinline__ void load(const void* base, size_t elem) {
+        raw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(base) + elem));
+    }
+    // plain (coherent) load, for data that this kernel also writes
+    __device__ __forceinline__ void load_rw(const void* base, size_t elem) {
+        raw = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(base) + elem);
+    }
+    __device__ __forceinline__ void store(void* base, size_t elem) const {
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + elem) = raw;
+    }
+    __device__ __forceinline__ float get(int j) const {
+        const uint32_t w = (&raw.x)[j >> 1];
+        return bf16_bits_to_float((j & 1) ? (w >> 16) : (w & 0xFFFFu));
+    }
+};
+
+template <> struct Act8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const void* base, size_t elem) {
+        const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + elem);
+        a = __ldg(p);
+        b = __ldg(p + 1);
+    }
+    __device__ __forceinline__ void load_rw(const void* base, size_t elem) {
+        const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + elem);
+        a = p[0];
+        b = p[1];
+    }
+    __device__ __forceinline__ void store(void* base, size_t elem) const {
+        float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + elem);
+        p[0] = a;
+        p[1] = b;
+    }
+    __device__ __forceinline__ float get(int j) const { return j < 4 ? (&a.x)[j] : (&b.x)[j - 4]; }
+};
+
+template <typename TA> __device__ __forceinline__ void store_act(void* base, size_t elem, float v);
+template <> __device__ __forceinline__ void store_act<bf16_t>(void* base, size_t elem, float v) {
+    reinterpret_cast<uint16_t*>(base)[elem] = float_to_bf16_bits(v);
+}
+template <> __device__ __forceinline__ void store_act<float>(void* base, size_t elem, float v) {
+    reinterpret_cast<float*>(base)[elem] = v;
+}
+
+template <typename TA> __device__ __forceinline__ float load_act(const void* base, size_t elem);
+template <> __device__ __forceinline__ float load_act<bf16_t>(const void* base, size_t elem) {
+    return bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(base) + elem));
+}
+template <> __device__ __forceinline__ float load_act<float>(const void* base, size_t elem) {
+    return __ldg(reinterpret_cast<const float*>(base) + elem);
+}
+
+// softplus(z) = log(1 + e^z), evaluated without overflow on either side.
+__device__ __forceinline__ float softplus_f32(float z) {
+    return z > 0.f ? z + log1pf(expf(-z)) : log1pf(expf(z));
+}
+
+// SiLU(u) = u * sigmoid(u) = u / (1 + e^-u); for u -> -inf it tends to -0.
+__device__ __forceinline__ float silu_f32(float u) { return u / (1.f + expf(-u)); }
+
+// Codes written to the device error word when a bounded wait runs out.
+enum : unsigned int {
+    ERR_NONE = 0,
+    ERR_MBAR_TIMEOUT_LOAD = 0x101,
+    ERR_MBAR_TIMEOUT_MMA = 0x102,
+    ERR_TMEM_ALLOC = 0x103,
+};
+
+}  // namespace m2

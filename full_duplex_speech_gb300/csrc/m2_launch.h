@@ -1,0 +1,52 @@
+// Host-side launchers of the mixer-core kernels, called by the C ABI layer
+// after it has validated every argument (m2_abi.cu). Each returns the
+// cudaError_t of its launches.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace m2 {
+
+struct Shape {
+    int H, P, N, G, K;
+    bool bf16;  // activation dtype: true = bf16, false = fp32
+    __host__ __device__ long HP() const { return (long)H * P; }
+    __host__ __device__ long GN() const { return (long)G * N; }
+    __host__ __device__ long CH() const { return HP() + 2 * GN(); }
+};
+
+struct StepArgs {
+    Shape s;
+    int S;  // sessions
+    const void *x, *B, *C, *dt_raw;
+    const float *A_log, *D, *dt_bias, *conv_w, *conv_b;
+    float* ssm;
+    void* conv;
+    void* y;
+    float* ws_u;   // [S, CH] post-conv, post-SiLU activations of this frame
+    float* ws_dt;  // [S, H] softplus'd step sizes
+};
+
+size_t step_workspace_bytes(const Shape& s, int S);
+cudaError_t launch_step(const StepArgs& a, cudaStream_t st);
+
+struct ScanArgs {
+    Shape s;
+    int batch, T, chunk;
+    const void *x, *B, *C, *dt_raw;
+    const float *A_log, *D, *dt_bias, *conv_w, *conv_b;
+    const float* init_ssm;
+    const void* init_conv;
+    void* y;
+    float* final_ssm;
+    void* final_conv;
+    void* ws;
+    size_t ws_bytes;
+    unsigned int* err;  // device error word
+};
+
+size_t scan_workspace_bytes(const Shape& s, int batch, int T, int chunk);
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t st);
+
+}  // namespace m2

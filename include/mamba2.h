@@ -1,0 +1,147 @@
+/*
+ * mamba2.h — C ABI of libmamba2.so, the GB300 (sm_103a) Mamba2 mixer core.
+ *
+ * The mixer core is the per-layer state-space part of each Mamba ('M') layer
+ * of the Nemotron-H language model inside NemotronLabs VoiceChat (issue
+ * "feat(nemotron_voicechat): load the VoiceChat checkpoint and run offline
+ * duplex inference", sections config.json / text_config and "Network 2";
+ * "docs/nemotron-voicechat.md", sections Offline timeline and Online
+ * session). Per layer it computes, for every frame t and head h (group
+ * g = h / (H/G)):
+ *
+ *   u_t      = SiLU(conv_b + sum_k conv_w[:,k] * xin_{t-(K-1)+k})   over x|B|C
+ *   dt_t,h   = softplus(dt_raw_t,h + dt_bias_h),   A_h = -exp(A_log_h)
+ *   h_t      = exp(dt A) h_{t-1} + dt x~_t (outer) B~_t,g
+ *   y_t      = h_t . C~_t,g + D_h x~_t
+ *
+ * (the Mamba-2 selective state-space recurrence, Dao & Gu 2024). It runs in
+ * two modes that must agree (VoiceChat doc, Offline timeline: recompute and
+ * cached mode give identical tokens):
+ *   mamba2_conv_scan — whole history / prefill, chunked (SSD) evaluation;
+ *   mamba2_step      — one frame for a batch of sessions from cached state.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.   Every pointer argument is DEVICE memory owned by the caller
+ *           (for instance from torch). The library allocates nothing on the
+ *           device and keeps no pointer after a call returns.
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *           All work is enqueued asynchronously on it; nothing synchronises.
+ * Errors.   Argument, shape and alignment checks happen on the host before
+ *           anything is enqueued; on failure nothing is launched and the
+ *           return value says why. A failed launch returns M2_ECUDA and
+ *           mamba2_last_cuda_error() gives the cudaError_t. Errors of kernels
+ *           already running surface at the caller's next synchronisation, as
+ *           for any CUDA work. Device-side waits are bounded: a wait that
+ *           runs out records a code readable with mamba2_device_error().
+ * Layouts.  Contiguous, innermost index last:
+ *             x [b,T,H,P]   B, C [b,T,G,N]   dt_raw [b,T,H]   y [b,T,H,P]
+ *             ssm state [b,H,P,N] fp32
+ *             conv tail [b,K-1,CH], oldest frame first, CH = H*P + 2*G*N,
+ *             channel order x | B | C (x at h*P+p, B at H*P+g*N+n,
+ *             C at H*P+G*N+g*N+n)
+ *             conv_w [CH,K] fp32 (the checkpoint's [CH,K,1] tensor read as
+ *             [CH,K]; a torch export [CH,1,K] has the same bytes)
+ *             conv_b [CH], A_log, D, dt_bias [H] fp32
+ *           The activation dtype (x, B, C, dt_raw, y, conv tail) is
+ *           m2_dims.act: bf16 or fp32.
+ * Alignment. Every pointer must be 16-byte aligned (M2_EALIGN otherwise).
+ * Shapes.   K == 4; N in {16, 32, 64, 128}; P a multiple of 16, at most 96;
+ *           H a multiple of G; H*P and G*N multiples of 8. (The Nemotron-H
+ *           mixer is H=128, P=80, N=128, G=8, K=4.) M2_ESHAPE otherwise.
+ */
+#ifndef MAMBA2_H
+#define MAMBA2_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    M2_OK = 0,
+    M2_EINVAL = 1,       /* a required pointer is NULL, or a count/size is negative or zero */
+    M2_ESHAPE = 2,       /* dimensions outside the supported set (see Shapes above) */
+    M2_EALIGN = 3,       /* a pointer is not 16-byte aligned */
+    M2_EUNSUPPORTED = 4, /* the current device is not an sm_103 GPU */
+    M2_ECUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+    M2_EWORKSPACE = 6    /* workspace is NULL or smaller than the query returned */
+} m2_status;
+
+typedef enum { M2_BF16 = 0, M2_F32 = 1 } m2_dtype;
+
+typedef struct {
+    int batch;     /* b: sequences in a scan (mamba2_step takes n_sessions instead) */
+    int T;         /* frames per sequence in a scan (ignored by mamba2_step) */
+    int nheads;    /* H, mamba_num_heads */
+    int headdim;   /* P, mamba_head_dim */
+    int dstate;    /* N, ssm_state_size */
+    int ngroups;   /* G, n_groups: B and C are shared by H/G consecutive heads */
+    int dconv;     /* K, conv_kernel (must be 4) */
+    m2_dtype act;  /* dtype of x, B, C, dt_raw, y and the conv tail */
+} m2_dims;
+
+/* Bytes of device scratch that mamba2_conv_scan needs for these dims and
+ * chunk length (0 if `d` or `chunk` is invalid). */
+size_t mamba2_scan_workspace_bytes(const m2_dims* d, int chunk);
+
+/* Whole-history (or prefill) evaluation of the mixer core over d->T frames
+ * of d->batch independent sequences, chunked in pieces of `chunk` frames
+ * (SSD form; 1 <= chunk <= 128; T need not be a multiple of it; results do
+ * not depend on it beyond rounding).
+ *
+ * Inputs : x, B, C, dt_raw (act dtype), A_log, D, dt_bias, conv_w, conv_b.
+ *          init_ssm [b,H,P,N] fp32 and init_conv [b,K-1,CH] (act dtype) are
+ *          the state to continue from; NULL means zeros (a fresh sequence).
+ * Outputs: y [b,T,H,P] (act dtype); final_ssm [b,H,P,N] fp32;
+ *          final_conv [b,K-1,CH] (act dtype): the last K-1 pre-conv input
+ *          frames, bit copies, taken from init_conv where T < K-1.
+ *          final_ssm and final_conv may alias init_ssm and init_conv (state
+ *          updated in place); no other output may alias any input.
+ * Scratch: workspace of at least mamba2_scan_workspace_bytes(d, chunk).
+ * T == 0 is valid: y is untouched and the final state equals the initial. */
+m2_status mamba2_conv_scan(const m2_dims* d, const void* x, const void* B, const void* C,
+                           const void* dt_raw, const float* A_log, const float* D,
+                           const float* dt_bias, const float* conv_w, const float* conv_b,
+                           int chunk, const float* init_ssm, const void* init_conv, void* y,
+                           float* final_ssm, void* final_conv, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Bytes of device scratch that mamba2_step needs for n_sessions sessions. */
+size_t mamba2_step_workspace_bytes(const m2_dims* d, int n_sessions);
+
+/* One cached frame for n_sessions independent sessions that share one
+ * layer's weights (the per-position update of the "Mamba2 state" that the
+ * VoiceChat online session keeps, "docs/nemotron-voicechat.md", section
+ * Online session).
+ *
+ * Inputs : this frame's x [S,H,P], B, C [S,G,N], dt_raw [S,H] (act dtype);
+ *          the layer's A_log, D, dt_bias, conv_w, conv_b.
+ * In/out : ssm_state [S,H,P,N] fp32 and conv_state [S,K-1,CH] (act dtype)
+ *          are read and updated in place.
+ * Output : y [S,H,P] (act dtype). y must not alias any input.
+ * Scratch: workspace of at least mamba2_step_workspace_bytes(d, S).
+ * d->batch and d->T are ignored. */
+m2_status mamba2_step(const m2_dims* d, int n_sessions, const void* x, const void* B,
+                      const void* C, const void* dt_raw, const float* A_log, const float* D,
+                      const float* dt_bias, const float* conv_w, const float* conv_b,
+                      float* ssm_state, void* conv_state, void* y, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Static description of a status code. */
+const char* mamba2_status_string(m2_status s);
+
+/* cudaError_t of the most recent M2_ECUDA returned on the calling thread. */
+int mamba2_last_cuda_error(void);
+
+/* Reads and clears the device-side error word of the current device
+ * (0 = no error; otherwise the code of a bounded wait that ran out).
+ * Synchronises `stream`. Returns M2_ECUDA if the read itself fails. */
+m2_status mamba2_device_error(void* stream, unsigned int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA2_H */

@@ -1,0 +1,94 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function
+include/mamba2.h declares, and rejects bad arguments before touching the
+GPU (these run without a GPU)."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def m2():
+    from full_duplex_speech_gb300 import build
+    build.build()
+    import full_duplex_speech_gb300 as m2
+    m2.load()
+    return m2
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "mamba2.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mamba2_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("mamba2_conv_scan", "mamba2_step", "mamba2_scan_workspace_bytes",
+              "mamba2_step_workspace_bytes", "mamba2_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(m2):
+    import ctypes
+    lib = ctypes.CDLL(m2.library_path())
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(m2):
+    for s in range(7):
+        assert m2.mamba2_status_string(s)
+    assert m2.mamba2_status_string(99) == "unknown status"
+
+
+def _fake_ptrs(n, base=1 << 20):
+    return [base + 256 * i for i in range(n)]
+
+
+def test_step_validation_without_gpu(m2):
+    d = m2.dims(0, 0, 4, 16, 16, 1, 4, "f32")
+    p = _fake_ptrs(12)
+    ws = m2.mamba2_step_workspace_bytes(d, 3)
+    assert ws > 0
+    ok = dict(workspace=1 << 30, workspace_bytes=ws, stream=0, check=False)
+    # a NULL input
+    assert m2.mamba2_step(d, 3, None, *p[1:], **ok) == 1
+    # negative session count
+    assert m2.mamba2_step(d, -1, *p, **ok) == 1
+    # misaligned pointer
+    assert m2.mamba2_step(d, 3, p[0] + 2, *p[1:], **ok) == 3
+    # workspace too small
+    assert m2.mamba2_step(d, 3, *p, workspace=1 << 30, workspace_bytes=ws - 1, stream=0, check=False) == 6
+    # unsupported dims: K != 4, N = 24, P = 20, H not a multiple of G
+    for bad in (m2.dims(0, 0, 4, 16, 16, 1, 3, "f32"), m2.dims(0, 0, 4, 16, 24, 1, 4, "f32"),
+                m2.dims(0, 0, 4, 20, 16, 1, 4, "f32"), m2.dims(0, 0, 6, 16, 16, 4, 4, "f32")):
+        assert m2.mamba2_step(bad, 3, *p, **ok) == 2
+    # zero heads is an invalid argument
+    assert m2.mamba2_step(m2.dims(0, 0, 0, 16, 16, 1, 4, "f32"), 3, *p, **ok) == 1
+
+
+def test_scan_validation_without_gpu(m2):
+    d = m2.dims(1, 64, 4, 16, 16, 1, 4, "f32")
+    p = _fake_ptrs(9)
+    outs = _fake_ptrs(3, base=1 << 24)
+    ok = dict(workspace=1 << 30, workspace_bytes=1 << 40, stream=0, check=False)
+    args = lambda chunk=16, ptrs=p: (d, *ptrs, chunk, None, None, *outs)  # noqa: E731
+    assert m2.mamba2_conv_scan(*args(0), **ok) == 1          # chunk < 1
+    assert m2.mamba2_conv_scan(*args(129), **ok) == 1        # chunk > 128
+    assert m2.mamba2_conv_scan(*args(16, [None] + p[1:]), **ok) == 1
+    assert m2.mamba2_conv_scan(*args(16, [p[0] + 8] + p[1:]), **ok) == 3
+    bad = m2.dims(1, 64, 4, 16, 16, 1, 5, "f32")
+    assert m2.mamba2_conv_scan(bad, *p, 16, None, None, *outs, **ok) == 2
+    neg = m2.dims(1, -1, 4, 16, 16, 1, 4, "f32")
+    assert m2.mamba2_conv_scan(neg, *p, 16, None, None, *outs, **ok) == 1
+
+
+def test_workspace_queries(m2):
+    d = m2.dims(4, 4096, 128, 80, 128, 8, 4, "bf16")
+    assert m2.mamba2_step_workspace_bytes(d, 64) >= 64 * (12288 + 128) * 4
+    assert m2.mamba2_step_workspace_bytes(d, -1) == 0
+    assert m2.mamba2_scan_workspace_bytes(d, 0) == 0
+    assert m2.mamba2_scan_workspace_bytes(m2.dims(1, 8, 4, 16, 16, 1, 3, "f32"), 8) == 0
