@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Benchmark of the Mamba2 mixer core on GB300.
+
+Workload: one Nemotron-H mixer at the real shape (H=128, P=80, N=128, G=8,
+K=4; bf16 activations, fp32 state), batch 1, a T=300-frame timeline (24 s at
+12.5 frames/s), chunk 128. One bench step is one pass of the whole hot path
+for one layer: the full-history chunked scan over the 300 frames (conv +
+SiLU, dt, SSD scan) followed by one cached single-frame step (frame 301) from
+the scan's final state. Steps cycle through 27 independently seeded layers
+(the Mamba layers of the 56-layer pattern), so the working set (~570 MB) is
+larger than L2 and no step reuses another's data from cache.
+
+value   = tokens per second = 301 frames x steps / device time (CUDA events).
+e2e     = the same metric through the C ABI with host buffers: pinned host ->
+          device copies of each step's inputs and device -> host copies of its
+          outputs inside the timed region.
+roofline: the dominant kernel (the fused SSD scan kernel, mamba2_scan_chunks),
+          algorithmic bytes per launch / its CUDA-event duration, against the
+          measured HBM copy bandwidth; a tensor-core figure is reported beside it.
+cpu_baseline / --impl reference: the fp64 oracle on the host cores.
+
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU with
+no data exchange (independent replicas, weak scaling); only the timing is
+reduced (max over ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from seeded_inputs import MAMBA_LAYERS, REAL_SHAPE, mixer_inputs  # noqa: E402
+
+T_FRAMES = 300
+CHUNK = 128
+N_LAYERS = len(MAMBA_LAYERS)
+METRIC = "Mamba2 scan tokens/s and per-frame step µs; % of HBM / bf16 MMA roofline"
+WORKLOAD = ("Nemotron-H Mamba2 mixer, real shape H=128 P=80 N=128 G=8 K=4, batch 1, T=300 chunked scan "
+            "(chunk 128) + 1 cached step, bf16 activations / fp32 state, 27 layers cycled")
+
+# Algorithmic work (per unit, stated in the design doc):
+#   scan bytes per token: x|B|C in 24,576 + dt 256 + y out 20,480 = 45,312 B
+#   plus the final fp32 state (H*P*N*4 = 5,242,880 B) and conv tail (3*12288*2) per sequence.
+#   scan MMA flops per token (dense, chunk 128): C.B^T 2*Q*N*G + M.x 2*Q*P*H + state 2*N*P*H
+#   + C.h 2*N*P*H = 8,126,464.
+#   step bytes per session: 2 x 5,242,880 state + 2 x 73,728 conv tail + 24,832 in + 20,480 out.
+SCAN_BYTES_PER_TOKEN = 45312
+STATE_BYTES = 128 * 80 * 128 * 4
+TAIL_BYTES = 3 * 12288 * 2
+SCAN_FLOPS_PER_TOKEN = 2 * CHUNK * 128 * 8 + 3 * (2 * 128 * 80 * 128)
+STEP_BYTES_PER_SESSION = 2 * STATE_BYTES + 2 * TAIL_BYTES + 24832 + 20480
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"], bf16_sust=j.get("bf16_tflops_sustained"),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for ts, r in rows if t0 - 0.1 <= ts <= t1 + 0.1] or [r for _, r in rows[-3:]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        sm = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (the only cross-rank operation)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- oracle leg
+def oracle_tokens_per_s(budget_s: float, nthreads: int, heads_cap=None):
+    """The fp64 oracle (as it stands) on one layer of the workload: the
+    T=301-frame recurrence (300 prefill frames + 1 cached frame; a cached step
+    is one more iteration of the same loop) for a sample of heads, timed
+    until `budget_s` seconds of work; tokens/s scaled to all 128 heads."""
+    import oracle
+    d = REAL_SHAPE
+    inp = mixer_inputs(1000, d, 1, T_FRAMES + 1, "bf16")
+    hs = 16 if heads_cap is None else heads_cap
+    t0 = time.perf_counter()
+    oracle.mixer_scan(d, inp, heads=(0, hs), nthreads=nthreads)
+    one = time.perf_counter() - t0
+    reps, elapsed = 1, one
+    while elapsed < budget_s:
+        t0 = time.perf_counter()
+        oracle.mixer_scan(d, inp, heads=(0, hs), nthreads=nthreads)
+        elapsed += time.perf_counter() - t0
+        reps += 1
+    per_rep = elapsed / reps
+    # hs heads took per_rep seconds: all 128 heads take per_rep * 128 / hs
+    value = (T_FRAMES + 1) / (per_rep * d.H / hs)
+    return value, dict(heads=hs, reps=reps, seconds=elapsed)
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the oracle timed on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    nthreads = os.cpu_count() or 1
+    # each step is a bounded sample: sized so that warmup + steps take ~2 minutes
+    budget_total = 120.0
+    d = REAL_SHAPE
+    inp = mixer_inputs(1000, d, 1, T_FRAMES + 1, "bf16")
+    t0 = time.perf_counter()
+    oracle.mixer_scan(d, inp, heads=(0, 8), nthreads=nthreads)
+    per_head = (time.perf_counter() - t0) / 8
+    per_step = budget_total / max(1, args.steps + args.warmup)
+    hs = int(max(1, min(d.H, per_step / max(per_head, 1e-9))))
+    hs = max(1, min(d.H, (hs // nthreads) * nthreads or hs))
+    for _ in range(args.warmup):
+        oracle.mixer_scan(d, inp, heads=(0, hs), nthreads=nthreads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.mixer_scan(d, inp, heads=(0, hs), nthreads=nthreads)
+        times.append(time.perf_counter() - t0)
+    ms = 1000.0 * sum(times) / len(times) * d.H / hs  # scaled to all 128 heads
+    value = (T_FRAMES + 1) / (ms / 1000.0)
+    sample = (f"per step: oracle fp64 recurrence over 301 frames for {hs} of 128 heads of one layer, "
+              f"scaled by 128/{hs}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; distributions of the tiny/real mixer configs)",
+            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": T_FRAMES + 1},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU leg
+class Layer:
+    """Device buffers of one layer: inputs for 301 frames, outputs, scratch."""
+
+    def __init__(self, m2, seed, torch, dev):
+        d = REAL_SHAPE
+        self.inp = mixer_inputs(seed, d, 1, T_FRAMES + 1, "bf16")
+
+        def dt(a):
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(a).to(dev)
+
+        full = {k: dt(self.inp[k]) for k in ("x", "B", "C", "dt_raw")}
+        self.seq = {k: v[:, :T_FRAMES].contiguous() for k, v in full.items()}
+        self.frame = {k: v[:, T_FRAMES].contiguous() for k, v in full.items()}
+        self.p = {k: dt(self.inp[k]) for k in ("A_log", "D", "dt_bias", "conv_w", "conv_b")}
+        self.dims = m2.dims(1, T_FRAMES, d.H, d.P, d.N, d.G, d.K, "bf16")
+        self.y = torch.empty((1, T_FRAMES, d.H, d.P), dtype=torch.bfloat16, device=dev)
+        self.y1 = torch.empty((1, d.H, d.P), dtype=torch.bfloat16, device=dev)
+        self.fs = torch.empty((1, d.H, d.P, d.N), dtype=torch.float32, device=dev)
+        self.fc = torch.empty((1, d.K - 1, d.CH), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(m2.mamba2_scan_workspace_bytes(self.dims, CHUNK), dtype=torch.uint8, device=dev)
+        self.wss = torch.empty(m2.mamba2_step_workspace_bytes(self.dims, 1), dtype=torch.uint8, device=dev)
+
+    def scan_args(self):
+        s, p = self.seq, self.p
+        return (self.dims, s["x"], s["B"], s["C"], s["dt_raw"], p["A_log"], p["D"], p["dt_bias"], p["conv_w"],
+                p["conv_b"], CHUNK, None, None, self.y, self.fs, self.fc, self.ws)
+
+    def step_args(self):
+        f, p = self.frame, self.p
+        return (self.dims, 1, f["x"], f["B"], f["C"], f["dt_raw"], p["A_log"], p["D"], p["dt_bias"],
+                p["conv_w"], p["conv_b"], self.fs, self.fc, self.y1, self.wss)
+
+
+def enqueue_step(m2, L, stream, ev=None):
+    """One bench step on `stream`: scan (prologue + SSD kernel) then one cached step.
+    ev = (a, b, c) events around the SSD kernel and the step call."""
+    m2.mamba2_scan_prepare_bc(*L.scan_args(), stream=stream)
+    if ev:
+        ev[0].record(stream)
+    m2.mamba2_scan_chunks(*L.scan_args(), stream=stream)
+    if ev:
+        ev[1].record(stream)
+    m2.mamba2_step(*L.step_args(), stream=stream)
+    if ev:
+        ev[2].record(stream)
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+    from full_duplex_speech_gb300 import build as m2build
+    m2build.build()
+    import full_duplex_speech_gb300 as m2
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    m2.load()
+    peaks = load_peaks()
+    layers = [Layer(m2, 1000 + i, torch, dev) for i in range(N_LAYERS)]
+    stream = torch.cuda.Stream(device=dev)
+    K, W = args.steps, args.warmup
+    torch.cuda.synchronize()
+
+    # warm-up (eager), then capture the timed sequence in CUDA graphs
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            enqueue_step(m2, layers[i % N_LAYERS], stream)
+    torch.cuda.synchronize()
+
+    try:
+        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
+        mk()
+        graph_events = True
+    except TypeError:
+        graph_events = False
+
+    sweep = min(K, N_LAYERS)
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) if graph_events else None for _ in range(3)]
+           for _ in range(sweep)]
+    g_full = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_full, stream=stream):
+        for i in range(sweep):
+            enqueue_step(m2, layers[i], stream, evs[i] if graph_events else None)
+    rem = K % sweep
+    g_rem = None
+    if rem:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rem, stream=stream):
+            for i in range(rem):
+                enqueue_step(m2, layers[i], stream)
+    g_full.replay()  # one untimed replay after capture
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0.record(stream)
+    for _ in range(K // sweep):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    time.sleep(0.2)
+    clocks.stop()
+    ms_local = e0.elapsed_time(e1)
+    ms_total = reduce_max(ms_local, world, dev)
+    ms_per_step = ms_total / K
+
+    # per-kernel durations: from the events inside the last full sweep of the timed region
+    if graph_events:
+        ssd_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(sweep)]
+        step_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(sweep)]
+        timing_src = "CUDA events captured in the replayed graph (last timed sweep)"
+    else:
+        ssd_ms, step_ms = [], []
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(sweep)]
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(50_000_000)  # keep the GPU busy while the host enqueues ahead
+            for i in range(sweep):
+                enqueue_step(m2, layers[i], stream, ev[i])
+        torch.cuda.synchronize()
+        ssd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(sweep)]
+        step_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(sweep)]
+        timing_src = "CUDA events on the launch stream (eager, host ahead of the GPU)"
+    ssd_avg = sum(ssd_ms) / len(ssd_ms)
+    step_avg = sum(step_ms) / len(step_ms)
+
+    ssd_bytes = SCAN_BYTES_PER_TOKEN * T_FRAMES + STATE_BYTES + TAIL_BYTES
+    ssd_gbs = ssd_bytes / (ssd_avg * 1e-3) / 1e9
+    ssd_flops = SCAN_FLOPS_PER_TOKEN * T_FRAMES
+    ssd_tfs = ssd_flops / (ssd_avg * 1e-3) / 1e12
+    step_gbs = STEP_BYTES_PER_SESSION / (step_avg * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers (eager, public calls)
+    e2e = None
+    if rank == 0 or True:
+        h_in = [{k: v.cpu().pin_memory() for k, v in {**L.seq, **{"f" + k: v for k, v in L.frame.items()}}.items()}
+                for L in layers]
+        h_out = [(torch.empty(L.y.shape, dtype=L.y.dtype).pin_memory(),
+                  torch.empty(L.y1.shape, dtype=L.y1.dtype).pin_memory()) for L in layers]
+        h2d = sum(v.numel() * v.element_size() for v in h_in[0].values())
+        d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+        ke = max(N_LAYERS, min(K, 4 * N_LAYERS))
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a0.record(stream)
+            for i in range(ke):
+                L = layers[i % N_LAYERS]
+                hi = h_in[i % N_LAYERS]
+                for k in ("x", "B", "C", "dt_raw"):
+                    L.seq[k].copy_(hi[k], non_blocking=True)
+                    L.frame[k].copy_(hi["f" + k], non_blocking=True)
+                enqueue_step(m2, L, stream)
+                h_out[i % N_LAYERS][0].copy_(L.y, non_blocking=True)
+                h_out[i % N_LAYERS][1].copy_(L.y1, non_blocking=True)
+            a1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(a0.elapsed_time(a1), world, dev) / ke
+        e2e = {"value": world * (T_FRAMES + 1) / (e2e_ms * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": ke}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nthreads = os.cpu_count() or 1
+        v, info = oracle_tokens_per_s(args.cpu_seconds, nthreads)
+        cpu = {"value": v, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+               "sample": (f"fp64 oracle, one layer: 301-frame recurrence (300 prefill + 1 cached) for "
+                          f"{info['heads']} of 128 heads, {info['reps']} reps in {info['seconds']:.1f} s, "
+                          f"scaled by 128/{info['heads']}")}
+
+    if rank == 0:
+        value = world * (T_FRAMES + 1) / (ms_per_step * 1e-3)
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded; no checkpoint or dataset)",
+            "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": T_FRAMES + 1,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2: 27 layer buffer sets (~570 MB) cycled"},
+            "roofline": {"bound": "hbm", "kernel": "scan_ssd_kernel (mamba2_scan_chunks)",
+                         "achieved": ssd_gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": ssd_gbs / peaks["hbm"], "traffic": args.ssd_traffic,
+                         "algorithmic_bytes_per_launch": ssd_bytes, "avg_launch_ms": ssd_avg,
+                         "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
+                         "timing": timing_src},
+            "roofline_tensor": {"kernel": "scan_ssd_kernel", "achieved": ssd_tfs, "peak": peaks["bf16"],
+                                "unit": "TFLOP/s", "frac": ssd_tfs / peaks["bf16"],
+                                "algorithmic_flops_per_launch": ssd_flops},
+            "step": {"us_per_layer_call": step_avg * 1e3, "us_per_frame_27_layers": step_avg * 1e3 * N_LAYERS,
+                     "achieved_gbs": step_gbs, "frac_hbm": step_gbs / peaks["hbm"],
+                     "bytes_per_call": STEP_BYTES_PER_SESSION, "sessions": 1},
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": 4 * K,
+            "clocks": clocks.summary(t_wall0, t_wall1),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5400)
+    ap.add_argument("--warmup", type=int, default=27)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ssd-traffic", type=float, default=None,
+                    help="ncu dram bytes per SSD launch, when a capture of the current kernel exists")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -53,8 +53,9 @@ def load():
         dp = ctypes.POINTER(M2Dims)
         lib.mamba2_scan_workspace_bytes.argtypes = [dp, ip]
         lib.mamba2_scan_workspace_bytes.restype = sz
-        lib.mamba2_conv_scan.argtypes = [dp] + [vp] * 9 + [ip] + [vp] * 6 + [sz, vp]
-        lib.mamba2_conv_scan.restype = ip
+        for f in ("mamba2_conv_scan", "mamba2_scan_prepare_bc", "mamba2_scan_chunks"):
+            getattr(lib, f).argtypes = [dp] + [vp] * 9 + [ip] + [vp] * 6 + [sz, vp]
+            getattr(lib, f).restype = ip
         lib.mamba2_step_workspace_bytes.argtypes = [dp, ip]
         lib.mamba2_step_workspace_bytes.restype = sz
         lib.mamba2_step.argtypes = [dp, ip] + [vp] * 13 + [sz, vp]
@@ -116,24 +117,47 @@ def mamba2_step_workspace_bytes(d: M2Dims, n_sessions: int) -> int:
     return load().mamba2_step_workspace_bytes(ctypes.byref(d), n_sessions)
 
 
-def mamba2_conv_scan(d: M2Dims, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk,
-                     init_ssm, init_conv, y, final_ssm, final_conv, workspace, workspace_bytes=None,
-                     stream=None, check=True) -> int:
+def _scan_call(fname, d, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk, init_ssm, init_conv,
+               y, final_ssm, final_conv, workspace, workspace_bytes, stream, check):
     if workspace_bytes is None:
-        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load().mamba2_conv_scan(
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
+    rc = getattr(load(), fname)(
         ctypes.byref(d), _p(x), _p(B), _p(C), _p(dt_raw), _p(A_log), _p(D), _p(dt_bias), _p(conv_w),
         _p(conv_b), int(chunk), _p(init_ssm), _p(init_conv), _p(y), _p(final_ssm), _p(final_conv),
         _p(workspace), int(workspace_bytes), _stream(stream))
     if check and rc:
-        raise M2Error(rc, "mamba2_conv_scan")
+        raise M2Error(rc, fname)
     return rc
+
+
+def mamba2_conv_scan(d: M2Dims, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk,
+                     init_ssm, init_conv, y, final_ssm, final_conv, workspace, workspace_bytes=None,
+                     stream=None, check=True) -> int:
+    return _scan_call("mamba2_conv_scan", d, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk,
+                      init_ssm, init_conv, y, final_ssm, final_conv, workspace, workspace_bytes, stream, check)
+
+
+def mamba2_scan_prepare_bc(d: M2Dims, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk,
+                           init_ssm, init_conv, y, final_ssm, final_conv, workspace, workspace_bytes=None,
+                           stream=None, check=True) -> int:
+    return _scan_call("mamba2_scan_prepare_bc", d, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b,
+                      chunk, init_ssm, init_conv, y, final_ssm, final_conv, workspace, workspace_bytes, stream,
+                      check)
+
+
+def mamba2_scan_chunks(d: M2Dims, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk,
+                       init_ssm, init_conv, y, final_ssm, final_conv, workspace, workspace_bytes=None,
+                       stream=None, check=True) -> int:
+    return _scan_call("mamba2_scan_chunks", d, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk,
+                      init_ssm, init_conv, y, final_ssm, final_conv, workspace, workspace_bytes, stream, check)
 
 
 def mamba2_step(d: M2Dims, n_sessions, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, ssm_state,
                 conv_state, y, workspace, workspace_bytes=None, stream=None, check=True) -> int:
     if workspace_bytes is None:
-        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
     rc = load().mamba2_step(
         ctypes.byref(d), int(n_sessions), _p(x), _p(B), _p(C), _p(dt_raw), _p(A_log), _p(D),
         _p(dt_bias), _p(conv_w), _p(conv_b), _p(ssm_state), _p(conv_state), _p(y), _p(workspace),

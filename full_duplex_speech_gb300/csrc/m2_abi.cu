@@ -159,12 +159,17 @@ size_t mamba2_scan_workspace_bytes(const m2_dims* d, int chunk) {
     return m2::scan_workspace_bytes(shape_of(d), d->batch, d->T, chunk);
 }
 
-m2_status mamba2_conv_scan(const m2_dims* d, const void* x, const void* B, const void* C,
-                           const void* dt_raw, const float* A_log, const float* D,
-                           const float* dt_bias, const float* conv_w, const float* conv_b,
-                           int chunk, const float* init_ssm, const void* init_conv, void* y,
-                           float* final_ssm, void* final_conv, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Validates a scan call and fills `a`. Returns M2_OK when there is work to
+// enqueue, or a status (M2_OK with a.batch == 0 means nothing to do).
+m2_status scan_setup(const m2_dims* d, const void* x, const void* B, const void* C, const void* dt_raw,
+                     const float* A_log, const float* D, const float* dt_bias, const float* conv_w,
+                     const float* conv_b, int chunk, const float* init_ssm, const void* init_conv, void* y,
+                     float* final_ssm, void* final_conv, void* workspace, size_t workspace_bytes,
+                     m2::ScanArgs* a) {
     m2_status st = check_dims(d, true);
     if (st != M2_OK) return st;
     if (chunk < 1 || chunk > 128) return M2_EINVAL;
@@ -185,31 +190,65 @@ m2_status mamba2_conv_scan(const m2_dims* d, const void* x, const void* B, const
     int dev = 0;
     st = current_device(&dev);
     if (st != M2_OK) return st;
-    if (d->batch == 0) return M2_OK;
+    a->s = s;
+    a->batch = d->batch;
+    a->T = d->T;
+    a->chunk = chunk;
+    a->x = x;
+    a->B = B;
+    a->C = C;
+    a->dt_raw = dt_raw;
+    a->A_log = A_log;
+    a->D = D;
+    a->dt_bias = dt_bias;
+    a->conv_w = conv_w;
+    a->conv_b = conv_b;
+    a->init_ssm = init_ssm;
+    a->init_conv = init_conv;
+    a->y = y;
+    a->final_ssm = final_ssm;
+    a->final_conv = final_conv;
+    a->ws = workspace;
+    a->ws_bytes = workspace_bytes;
+    a->err = g_dev_error_ptr[dev];
+    return M2_OK;
+}
 
+}  // namespace
+
+#define M2_SCAN_PARAMS                                                                              \
+    const m2_dims *d, const void *x, const void *B, const void *C, const void *dt_raw,              \
+        const float *A_log, const float *D, const float *dt_bias, const float *conv_w,              \
+        const float *conv_b, int chunk, const float *init_ssm, const void *init_conv, void *y,      \
+        float *final_ssm, void *final_conv, void *workspace, size_t workspace_bytes, void *stream
+#define M2_SCAN_ARGS                                                                                 \
+    d, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk, init_ssm, init_conv, y, final_ssm, \
+        final_conv, workspace, workspace_bytes
+
+extern "C" {
+
+m2_status mamba2_scan_prepare_bc(M2_SCAN_PARAMS) {
     m2::ScanArgs a;
-    a.s = s;
-    a.batch = d->batch;
-    a.T = d->T;
-    a.chunk = chunk;
-    a.x = x;
-    a.B = B;
-    a.C = C;
-    a.dt_raw = dt_raw;
-    a.A_log = A_log;
-    a.D = D;
-    a.dt_bias = dt_bias;
-    a.conv_w = conv_w;
-    a.conv_b = conv_b;
-    a.init_ssm = init_ssm;
-    a.init_conv = init_conv;
-    a.y = y;
-    a.final_ssm = final_ssm;
-    a.final_conv = final_conv;
-    a.ws = workspace;
-    a.ws_bytes = workspace_bytes;
-    a.err = g_dev_error_ptr[dev];
-    cudaError_t e = m2::launch_scan(a, static_cast<cudaStream_t>(stream));
+    m2_status st = scan_setup(M2_SCAN_ARGS, &a);
+    if (st != M2_OK || d->batch == 0) return st;
+    cudaError_t e = m2::launch_scan_prepare(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M2_OK : cuda_fail(e);
+}
+
+m2_status mamba2_scan_chunks(M2_SCAN_PARAMS) {
+    m2::ScanArgs a;
+    m2_status st = scan_setup(M2_SCAN_ARGS, &a);
+    if (st != M2_OK || d->batch == 0) return st;
+    cudaError_t e = m2::launch_scan_chunks(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M2_OK : cuda_fail(e);
+}
+
+m2_status mamba2_conv_scan(M2_SCAN_PARAMS) {
+    m2::ScanArgs a;
+    m2_status st = scan_setup(M2_SCAN_ARGS, &a);
+    if (st != M2_OK || d->batch == 0) return st;
+    cudaError_t e = m2::launch_scan_prepare(a, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = m2::launch_scan_chunks(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M2_OK : cuda_fail(e);
 }
 

@@ -47,6 +47,9 @@ struct ScanArgs {
 };
 
 size_t scan_workspace_bytes(const Shape& s, int batch, int T, int chunk);
-cudaError_t launch_scan(const ScanArgs& a, cudaStream_t st);
+// B/C conv prologue into the workspace tiles (first half of a scan).
+cudaError_t launch_scan_prepare(const ScanArgs& a, cudaStream_t st);
+// Fused chunked SSD over prepared tiles, final state and conv tail (second half).
+cudaError_t launch_scan_chunks(const ScanArgs& a, cudaStream_t st);
 
 }  // namespace m2

@@ -1,5 +1,5 @@
 // Chunked (SSD) scan of the Mamba2 mixer core: full-history recompute and
-// prefill. Three kernels per call, on the caller's stream:
+// prefill. Two kernels per call, on the caller's stream:
 //
 //  1. scan_bc_kernel  — causal conv + SiLU of the B and C channels (shared by
 //     the H/G heads of a group), written once per (sequence, chunk, group) as
@@ -17,7 +17,8 @@
 //        y       = M x~ + exp(S_i) Y_off + D x~              (tcgen05, bf16)
 //     The conv + SiLU of the head's own x channels, softplus(dt) and the
 //     cumulative sums run on the CUDA cores between the tensor-core phases.
-//  3. scan_tail_kernel — the final conv tail (the last K-1 pre-conv frames).
+//     At its end each CTA also writes its share of the final conv tail (the
+//     last K-1 pre-conv frames).
 //
 // The chunked form is the state-space-duality (SSD) evaluation of the Mamba-2
 // recurrence (Dao & Gu 2024): the intra-chunk part is a masked quadratic form,
@@ -123,6 +124,40 @@ __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nch
         } else {
             *reinterpret_cast<uint4*>(tCh + off) = hi;
         }
+    }
+}
+
+// The final conv tail of 8 channels [c, c+8) of sequence b: frames T-3..T-1,
+// taken from the initial tail (or zeros) where T < 3. Every source slot is
+// read before any is written, so final_conv may alias init_conv.
+template <typename TA>
+__device__ void write_tail(const ScanArgs& a, int b, long c) {
+    const Shape& s = a.s;
+    const long CH = s.CH(), HP = s.HP(), GN = s.GN();
+    const int T = a.T;
+    Act8<TA> vals[3];
+    bool zero[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const int t = T - 3 + k;
+        zero[k] = false;
+        if (t >= 0) {
+            if (c < HP)
+                vals[k].load(a.x, ((size_t)b * T + t) * HP + c);
+            else if (c < HP + GN)
+                vals[k].load(a.B, ((size_t)b * T + t) * GN + (c - HP));
+            else
+                vals[k].load(a.C, ((size_t)b * T + t) * GN + (c - HP - GN));
+        } else if (a.init_conv) {
+            vals[k].load_rw(a.init_conv, ((size_t)b * 3 + (3 + t)) * CH + c);
+        } else {
+            zero[k] = true;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        if (zero[k]) memset(&vals[k], 0, sizeof(vals[k]));
+        vals[k].store(a.final_conv, ((size_t)b * 3 + k) * CH + c);
     }
 }
 
@@ -482,77 +517,66 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         tc::mbar_wait(bar_ld, 0, 100000000ull);
         tc::mbar_wait(bar_ld, 1, 100000000ull);
     }
+    // final conv tail (the last K-1 pre-conv frames). This CTA owns the tail of
+    // its head's x channels (whose initial frames only it has read); the first
+    // head of each group also owns the group's B and C channels (whose initial
+    // frames only the prologue kernel read). So in-place updates are safe.
+    {
+        const int R = s.H / s.G;
+        const int nx = P / 8, nbc = (h % R == 0) ? 2 * s.N / 8 : 0;
+        for (int v = tid; v < nx + nbc; v += kSsdThreads) {
+            long c;
+            if (v < nx)
+                c = (long)h * P + v * 8;
+            else if (v - nx < s.N / 8)
+                c = HP + (long)g * s.N + (v - nx) * 8;
+            else
+                c = HP + s.GN() + (long)g * s.N + (v - nx - s.N / 8) * 8;
+            write_tail<TA>(a, b, c);
+        }
+    }
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, kTmemCols);
 }
 
-// ----------------------------------------------------------------- kernel 3
-template <typename TA>
-__global__ void scan_tail_kernel(ScanArgs a) {
-    const Shape& s = a.s;
-    const long CH = s.CH(), HP = s.HP(), GN = s.GN();
-    const long nvec = CH / 8;
-    const long v = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    const int b = blockIdx.y;
-    if (v >= nvec) return;
-    const long c = v * 8;
-    const int T = a.T;
-    // read every source slot before writing: final_conv may alias init_conv
-    Act8<TA> vals[3];
-    bool zero[3];
-    for (int k = 0; k < 3; ++k) {
-        const int t = T - 3 + k;
-        zero[k] = false;
-        if (t >= 0) {
-            if (c < HP)
-                vals[k].load(a.x, ((size_t)b * T + t) * HP + c);
-            else if (c < HP + GN)
-                vals[k].load(a.B, ((size_t)b * T + t) * GN + (c - HP));
-            else
-                vals[k].load(a.C, ((size_t)b * T + t) * GN + (c - HP - GN));
-        } else if (a.init_conv) {
-            vals[k].load_rw(a.init_conv, ((size_t)b * 3 + (3 + t)) * CH + c);
-        } else {
-            zero[k] = true;
-        }
-    }
-    for (int k = 0; k < 3; ++k) {
-        if (zero[k]) memset(&vals[k], 0, sizeof(vals[k]));
-        vals[k].store(a.final_conv, ((size_t)b * 3 + k) * CH + c);
-    }
-}
-
 template <typename TA, int P>
 cudaError_t launch_ssd(const ScanArgs& a, int nchunks, cudaStream_t st) {
     const int smem = SsdSmem<P>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(scan_ssd_kernel<TA, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // once per process and instantiation (kept out of graph captures after the first call)
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(scan_ssd_kernel<TA, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
     scan_ssd_kernel<TA, P><<<dim3(a.s.H, a.batch), kSsdThreads, smem, st>>>(a, nchunks);
     return cudaGetLastError();
 }
 
 template <typename TA>
-cudaError_t launch_typed(const ScanArgs& a, cudaStream_t st) {
+cudaError_t launch_bc_typed(const ScanArgs& a, cudaStream_t st) {
     const int nchunks = (a.T + a.chunk - 1) / a.chunk;
-    cudaError_t e;
-    if (nchunks > 0) {
-        scan_bc_kernel<TA><<<dim3(nchunks, a.s.G, a.batch), kBcThreads, 0, st>>>(a, nchunks);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if (nchunks == 0) return cudaSuccess;
+    scan_bc_kernel<TA><<<dim3(nchunks, a.s.G, a.batch), kBcThreads, 0, st>>>(a, nchunks);
+    return cudaGetLastError();
+}
+
+template <typename TA>
+cudaError_t launch_chunks_typed(const ScanArgs& a, cudaStream_t st) {
+    const int nchunks = (a.T + a.chunk - 1) / a.chunk;
     switch (a.s.P) {
-        case 16: e = launch_ssd<TA, 16>(a, nchunks, st); break;
-        case 32: e = launch_ssd<TA, 32>(a, nchunks, st); break;
-        case 48: e = launch_ssd<TA, 48>(a, nchunks, st); break;
-        case 64: e = launch_ssd<TA, 64>(a, nchunks, st); break;
-        case 80: e = launch_ssd<TA, 80>(a, nchunks, st); break;
-        case 96: e = launch_ssd<TA, 96>(a, nchunks, st); break;
+        case 16: return launch_ssd<TA, 16>(a, nchunks, st);
+        case 32: return launch_ssd<TA, 32>(a, nchunks, st);
+        case 48: return launch_ssd<TA, 48>(a, nchunks, st);
+        case 64: return launch_ssd<TA, 64>(a, nchunks, st);
+        case 80: return launch_ssd<TA, 80>(a, nchunks, st);
+        case 96: return launch_ssd<TA, 96>(a, nchunks, st);
         default: return cudaErrorInvalidValue;
     }
-    if (e != cudaSuccess) return e;
-    const long nvec = a.s.CH() / 8;
-    scan_tail_kernel<TA><<<dim3((unsigned)((nvec + 255) / 256), a.batch), 256, 0, st>>>(a);
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -563,9 +587,14 @@ size_t scan_workspace_bytes(const Shape& s, int batch, int T, int chunk) {
     return (size_t)batch * nchunks * s.G * 3 * kTileBytes;
 }
 
-cudaError_t launch_scan(const ScanArgs& a, cudaStream_t st) {
+cudaError_t launch_scan_prepare(const ScanArgs& a, cudaStream_t st) {
     if (a.batch == 0) return cudaSuccess;
-    return a.s.bf16 ? launch_typed<bf16_t>(a, st) : launch_typed<float>(a, st);
+    return a.s.bf16 ? launch_bc_typed<bf16_t>(a, st) : launch_bc_typed<float>(a, st);
+}
+
+cudaError_t launch_scan_chunks(const ScanArgs& a, cudaStream_t st) {
+    if (a.batch == 0) return cudaSuccess;
+    return a.s.bf16 ? launch_chunks_typed<bf16_t>(a, st) : launch_chunks_typed<float>(a, st);
 }
 
 }  // namespace m2

@@ -108,6 +108,31 @@ m2_status mamba2_conv_scan(const m2_dims* d, const void* x, const void* B, const
                            float* final_ssm, void* final_conv, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* The two halves of mamba2_conv_scan, with the same arguments, for callers
+ * that schedule or time them separately. mamba2_conv_scan(args) is exactly
+ * mamba2_scan_prepare_bc(args) followed by mamba2_scan_chunks(args) on the
+ * same stream.
+ *   mamba2_scan_prepare_bc: causal conv + SiLU of the B and C channels into
+ *     the workspace as tensor-core operand tiles. Reads B, C, conv_w, conv_b,
+ *     init_conv; writes only the workspace.
+ *   mamba2_scan_chunks: the chunked SSD evaluation over those tiles, with the
+ *     head's own x-channel conv, dt, y, final_ssm and final_conv. It must run
+ *     after mamba2_scan_prepare_bc with the same B, C, conv weights,
+ *     init_conv, chunk and workspace, and before the workspace is reused.
+ * Validation and error behaviour are those of mamba2_conv_scan. */
+m2_status mamba2_scan_prepare_bc(const m2_dims* d, const void* x, const void* B, const void* C,
+                                 const void* dt_raw, const float* A_log, const float* D,
+                                 const float* dt_bias, const float* conv_w, const float* conv_b,
+                                 int chunk, const float* init_ssm, const void* init_conv, void* y,
+                                 float* final_ssm, void* final_conv, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+m2_status mamba2_scan_chunks(const m2_dims* d, const void* x, const void* B, const void* C,
+                             const void* dt_raw, const float* A_log, const float* D,
+                             const float* dt_bias, const float* conv_w, const float* conv_b,
+                             int chunk, const float* init_ssm, const void* init_conv, void* y,
+                             float* final_ssm, void* final_conv, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 /* Bytes of device scratch that mamba2_step needs for n_sessions sessions. */
 size_t mamba2_step_workspace_bytes(const m2_dims* d, int n_sessions);
 
