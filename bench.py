@@ -310,7 +310,8 @@ def run_gpu(args, world, rank, local):
         with torch.cuda.graph(g_rem, stream=stream):
             for i in range(rem):
                 enqueue_step(m2, layers[i], stream)
-    g_full.replay()  # one untimed replay after capture
+    with torch.cuda.stream(stream):  # CUDAGraph.replay() launches on the current stream
+        g_full.replay()  # one untimed replay after capture
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
@@ -320,12 +321,13 @@ def run_gpu(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    e0.record(stream)
-    for _ in range(K // sweep):
-        g_full.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K // sweep):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     barrier(world)

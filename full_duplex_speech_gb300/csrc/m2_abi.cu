@@ -53,7 +53,7 @@ m2_status check_dims(const m2_dims* d, bool need_seq) {
     if (d->dconv != 4) return M2_ESHAPE;
     const int N = d->dstate;
     if (N != 16 && N != 32 && N != 64 && N != 128) return M2_ESHAPE;
-    if (d->headdim % 16 != 0 || d->headdim > 96) return M2_ESHAPE;
+    if (d->headdim % 16 != 0 || d->headdim > 80) return M2_ESHAPE;
     if (d->nheads % d->ngroups != 0) return M2_ESHAPE;
     if (((long)d->nheads * d->headdim) % 8 != 0 || ((long)d->ngroups * N) % 8 != 0) return M2_ESHAPE;
     return M2_OK;

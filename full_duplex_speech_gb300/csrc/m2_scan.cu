@@ -23,7 +23,9 @@
 // The chunked form is the state-space-duality (SSD) evaluation of the Mamba-2
 // recurrence (Dao & Gu 2024): the intra-chunk part is a masked quadratic form,
 // the carried state enters through C~ h_prev.
+#include <cuda.h>
 #include <math.h>
+#include <string.h>
 
 #include "m2_common.cuh"
 #include "m2_launch.h"
@@ -40,11 +42,12 @@ constexpr uint32_t kPanel = kTR * 128;          // one 64-column panel of a tile
 
 // ----------------------------------------------------------------- kernel 1
 constexpr int kBcThreads = 256;
+constexpr int kBcRows = 4;  // rows per thread; a CTA covers 32 rows of one (chunk, group)
 
 template <typename TA>
 __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nchunks) {
     const Shape& s = a.s;
-    const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int c = blockIdx.x >> 2, quarter = blockIdx.x & 3, g = blockIdx.y, b = blockIdx.z;
     const int T = a.T, Q = a.chunk;
     const int c0 = c * Q;
     const int L = min(Q, T - c0);
@@ -54,70 +57,64 @@ __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nch
     uint8_t* tBl = tiles + kTileBytes;
     uint8_t* tCh = tiles + 2 * kTileBytes;
 
-    // 32 columns of 8 channels: 16 for B (n = 0..127), 16 for C; 8 row segments of 16.
+    // 32 columns of 8 channels (16 for B, 16 for C) x 8 groups of 4 rows.
     const int cc = threadIdx.x & 31, rs = threadIdx.x >> 5;
     const int which = cc >> 4;  // 0: B, 1: C
     const int n0 = (cc & 15) * 8;
-    const int r0 = rs * 16;
+    const int r0 = quarter * 32 + rs * kBcRows;
     const bool real = n0 < s.N;
     const long ch0 = HP + which * GN + (long)g * s.N + n0;  // conv channel of n0
     const void* src = which ? a.C : a.B;
+    pdl_wait();  // B and C may come from the previous kernel
 
-    float w[8][4], bias[8];
-    if (real) {
+    float out[kBcRows][8];
+    if (real && r0 < L) {
+        // pre-conv rows r0-3 .. r0+3, all loads issued before any use
+        float win[kBcRows + 3][8];
+#pragma unroll
+        for (int k = 0; k < kBcRows + 3; ++k) {
+            const int t = c0 + r0 - 3 + k;
+            Act8<TA> v;
+            bool have = true;
+            if (t >= 0 && t < c0 + L)
+                v.load(src, (((size_t)b * T + t) * s.G + g) * s.N + n0);
+            else if (t < 0 && a.init_conv)
+                v.load(a.init_conv, ((size_t)b * (s.K - 1) + (s.K - 1 + t)) * CH + ch0);
+            else
+                have = false;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) win[k][j] = have ? v.get(j) : 0.f;
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float4 wj = __ldg(reinterpret_cast<const float4*>(a.conv_w) + ch0 + j);
-            w[j][0] = wj.x; w[j][1] = wj.y; w[j][2] = wj.z; w[j][3] = wj.w;
-            bias[j] = __ldg(a.conv_b + ch0 + j);
+            const float bj = __ldg(a.conv_b + ch0 + j);
+#pragma unroll
+            for (int r = 0; r < kBcRows; ++r) {
+                float u = bj;
+                u = fmaf(wj.x, win[r][j], u);
+                u = fmaf(wj.y, win[r + 1][j], u);
+                u = fmaf(wj.z, win[r + 2][j], u);
+                u = fmaf(wj.w, win[r + 3][j], u);
+                out[r][j] = silu_fast(u);
+            }
         }
     }
-    // sliding window of pre-conv rows t-3, t-2, t-1
-    float win[3][8];
-    auto load_row = [&](int t, float (&out)[8]) {
-        if (t >= 0 && t < T) {
-            Act8<TA> v;
-            v.load(src, (((size_t)b * T + t) * s.G + g) * s.N + n0);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) out[j] = v.get(j);
-        } else if (t < 0 && a.init_conv) {
-            Act8<TA> v;
-            v.load(a.init_conv, ((size_t)b * (s.K - 1) + (s.K - 1 + t)) * CH + ch0);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) out[j] = v.get(j);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) out[j] = 0.f;
-        }
-    };
-    if (real && r0 < L) {
-#pragma unroll
-        for (int k = 0; k < 3; ++k) load_row(c0 + r0 - 3 + k, win[k]);
-    }
-    for (int r = r0; r < r0 + 16; ++r) {
+    for (int r = 0; r < kBcRows; ++r) {
+        const int row = r0 + r;
         uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-        if (real && r < L) {
-            float cur[8];
-            load_row(c0 + r, cur);
+        if (real && row < L) {
             uint32_t hb[8], lb[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                float u = bias[j];
-                u = fmaf(w[j][0], win[0][j], u);
-                u = fmaf(w[j][1], win[1][j], u);
-                u = fmaf(w[j][2], win[2][j], u);
-                u = fmaf(w[j][3], cur[j], u);
-                const float v = silu_f32(u);
-                hb[j] = float_to_bf16_bits(v);
-                lb[j] = float_to_bf16_bits(v - bf16_bits_to_float(hb[j]));
-                win[0][j] = win[1][j];
-                win[1][j] = win[2][j];
-                win[2][j] = cur[j];
+                hb[j] = float_to_bf16_bits(out[r][j]);
+                lb[j] = float_to_bf16_bits(out[r][j] - bf16_bits_to_float(hb[j]));
             }
             hi = make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16), hb[6] | (hb[7] << 16));
             lo = make_uint4(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16), lb[4] | (lb[5] << 16), lb[6] | (lb[7] << 16));
         }
-        const uint32_t off = tc::sw128_off(r, n0, kTR);
+        const uint32_t off = tc::sw128_off(row, n0, kTR);
         if (which == 0) {
             *reinterpret_cast<uint4*>(tBh + off) = hi;
             *reinterpret_cast<uint4*>(tBl + off) = lo;
@@ -125,6 +122,7 @@ __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nch
             *reinterpret_cast<uint4*>(tCh + off) = hi;
         }
     }
+    pdl_trigger();  // at the end, so waiting SSD CTAs do not crowd this grid off the SMs
 }
 
 // The final conv tail of 8 channels [c, c+8) of sequence b: frames T-3..T-1,
@@ -163,10 +161,11 @@ __device__ void write_tail(const ScanArgs& a, int b, long c) {
 
 // ----------------------------------------------------------------- kernel 2
 constexpr int kSsdThreads = 256;
+constexpr int kRawRows = kTR + 3;  // pre-conv rows of one chunk plus the 3-frame halo
 // TMEM columns
 constexpr uint32_t kColG = 0, kColState = 128, kColYd = 256, kColYo = 384, kTmemCols = 512;
 
-template <int P>
+template <typename TA, int P>
 struct SsdSmem {
     static constexpr uint32_t kC = 0;                     // C~ hi           (K-major SW128)
     static constexpr uint32_t kBh = kTileBytes;           // B~ hi           (K-major / MN-major SW128)
@@ -176,13 +175,15 @@ struct SsdSmem {
     static constexpr uint32_t kWh = kX + kPT;             // (w o x~) hi
     static constexpr uint32_t kWl = kWh + kPT;            // (w o x~) lo
     static constexpr uint32_t kH = kWl + kPT;             // h hi            (MN-major interleave, K = n)
-    static constexpr uint32_t kS = kH + kPT;              // float S[128]
+    static constexpr uint32_t kRaw = kH + kPT;            // pre-conv x rows [kRawRows][P] (act dtype)
+    static constexpr uint32_t kRowBytes = P * sizeof(TA);
+    static constexpr uint32_t kS = kRaw + kRawRows * kRowBytes;  // float S[128]
     static constexpr uint32_t kDt = kS + 512;             // float dt[128]
     static constexpr uint32_t kWsum = kDt + 512;          // float warp sums[8]
     static constexpr uint32_t kCw = kWsum + 64;           // float conv_w[P][4]
     static constexpr uint32_t kCb = kCw + P * 16;         // float conv_b[P]
-    static constexpr uint32_t kBar = (kCb + P * 4 + 15) / 16 * 16;  // 3 mbarriers
-    static constexpr uint32_t kTmem = kBar + 24;          // TMEM base address
+    static constexpr uint32_t kBar = (kCb + P * 4 + 15) / 16 * 16;  // 6 mbarriers
+    static constexpr uint32_t kTmem = kBar + 48;          // TMEM base address
     static constexpr uint32_t kFlag = kTmem + 4;          // abort flag
     static constexpr uint32_t kBytes = kFlag + 4 + 1024;  // + slack to align the base to 1024
 };
@@ -191,10 +192,24 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return (uint32_t)float_to_bf16_bits(a) | ((uint32_t)float_to_bf16_bits(b) << 16);
 }
 
+// Stages the pre-conv x rows of chunk c (frames c0-3 .. c0+kTR-1) of this head
+// into shared memory with one 3-D TMA box copy of [kRawRows frames x P
+// channels]; frames outside [0, T) read as zero (the caller patches the three
+// frames before the sequence from the initial conv tail, when there is one).
 template <typename TA, int P>
-__global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, int nchunks) {
-    using L = SsdSmem<P>;
-    constexpr int PH = P / 2;  // columns handled by each half of the CTA
+__device__ __forceinline__ void stage_raw_x(const CUtensorMap* tmx, uint8_t* raw, uint64_t* bar, int b, int h,
+                                            int c0) {
+    using Lay = SsdSmem<TA, P>;
+    tc::mbar_arrive_expect_tx(bar, (uint32_t)kRawRows * Lay::kRowBytes);
+    tc::tma_load_3d(raw, tmx, h * P, c0 - 3, b, bar);
+}
+
+template <typename TA, int P>
+__global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, int nchunks,
+                                                                  const __grid_constant__ CUtensorMap tmx) {
+    using L = SsdSmem<TA, P>;
+    constexpr int PH = P / 2;   // columns handled by each half of the CTA
+    constexpr int NQ = PH / 8;  // 8-column groups per half
     constexpr uint32_t LBO_I = (P / 8) * 128;  // K-group stride of the interleaved tiles
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -203,8 +218,8 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     const int h = blockIdx.x, b = blockIdx.y;
     const int g = h / (s.H / s.G);
     const int T = a.T, Q = a.chunk;
-    const long HP = s.HP(), CH = s.CH();
-    const int tid = threadIdx.x, row = tid & 127, half = tid >> 7, warp = tid >> 5;
+    const long HP = s.HP();
+    const int tid = threadIdx.x, row = tid & 127, half = tid >> 7, warp = tid >> 5, lane = tid & 31;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     float* sS = reinterpret_cast<float*>(sm + L::kS);
@@ -212,16 +227,18 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     float* sWsum = reinterpret_cast<float*>(sm + L::kWsum);
     float* sCw = reinterpret_cast<float*>(sm + L::kCw);
     float* sCb = reinterpret_cast<float*>(sm + L::kCb);
-    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + L::kBar);
-    uint64_t* bar_m1 = bar_ld + 1;
-    uint64_t* bar_m2 = bar_ld + 2;
+    uint8_t* sRaw = sm + L::kRaw;
+    uint64_t* bar_a = reinterpret_cast<uint64_t*>(sm + L::kBar);  // C~ hi + B~ hi tiles
+    uint64_t* bar_b = bar_a + 1;                                   // B~ lo tile
+    uint64_t* bar_x = bar_a + 2;                                   // pre-conv x rows
+    uint64_t* bar_g = bar_a + 3;                                   // G done
+    uint64_t* bar_bl = bar_a + 4;                                  // state terms reading B~ lo done
+    uint64_t* bar_y = bar_a + 5;                                   // every MMA of the chunk done
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::kTmem);
     volatile uint32_t* sFlag = reinterpret_cast<uint32_t*>(sm + L::kFlag);
 
     if (tid == 0) {
-        tc::mbar_init(bar_ld, 1);
-        tc::mbar_init(bar_m1, 1);
-        tc::mbar_init(bar_m2, 1);
+        for (int i = 0; i < 6; ++i) tc::mbar_init(bar_a + i, 1);
         tc::fence_mbar_init();
         *sFlag = 0;
     }
@@ -245,7 +262,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     // initial state -> TMEM [n lanes][p columns]; rows n >= N stay zero
     {
         const int n = row;
-        for (int p0 = half * PH; p0 < (half + 1) * PH; p0 += 8) {
+#pragma unroll
+        for (int q8 = 0; q8 < NQ; ++q8) {
+            const int p0 = half * PH + q8 * 8;
             float v[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -256,39 +275,53 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         }
         tc::tmem_wait_st();
     }
+    // first chunk's pre-conv x rows and dt_raw (inputs written before the prologue kernel)
+    if (nchunks > 0 && tid == 32) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, 0);
+    float dt_raw_next = 0.f;
+    if (nchunks > 0 && half == 0 && row < min(Q, T))
+        dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + row) * s.H + h);
 
     const uint32_t sbase = tc::smem_u32(sm);
     const uint8_t* ws = reinterpret_cast<const uint8_t*>(a.ws);
+    auto tiles_of = [&](int c) { return ws + (((size_t)b * nchunks + c) * s.G + g) * 3 * kTileBytes; };
     bool ok = true;
+    // the operand tiles are the prologue kernel's output
+    pdl_wait();
+    if (nchunks > 0 && tid == 0) {
+        const uint8_t* src = tiles_of(0);
+        tc::mbar_arrive_expect_tx(bar_a, 2 * kTileBytes);
+        tc::bulk_g2s(sm + L::kBh, src, kTileBytes, bar_a);
+        tc::bulk_g2s(sm + L::kC, src + 2 * kTileBytes, kTileBytes, bar_a);
+        tc::mbar_arrive_expect_tx(bar_b, kTileBytes);
+        tc::bulk_g2s(sm + L::kBl, src + kTileBytes, kTileBytes, bar_b);
+    }
 
     for (int c = 0; c < nchunks; ++c) {
         const int c0 = c * Q;
         const int Lc = min(Q, T - c0);
         const int ksteps = (Lc + 15) / 16;
         const uint32_t par = c & 1;
+        const bool has_next = c + 1 < nchunks;
+        const int Ln = has_next ? min(Q, T - c0 - Q) : 0;
 
-        // 1. B~/C~ tiles of this chunk and group: bulk copy into shared memory
-        if (tid == 0) {
-            const uint8_t* src = ws + (((size_t)b * nchunks + c) * s.G + g) * 3 * kTileBytes;
-            tc::mbar_arrive_expect_tx(bar_ld, 3 * kTileBytes);
-            tc::bulk_g2s(sm + L::kBh, src, kTileBytes, bar_ld);
-            tc::bulk_g2s(sm + L::kBl, src + kTileBytes, kTileBytes, bar_ld);
-            tc::bulk_g2s(sm + L::kC, src + 2 * kTileBytes, kTileBytes, bar_ld);
-        }
-
-        // 2. dt, a = dt A, inclusive cumulative sum S over the chunk
+        // 1. dt = softplus(dt_raw + dt_bias), a = dt A, inclusive cumulative sum S
         if (half == 0) {
-            float dt = 0.f;
-            if (row < Lc) dt = softplus_f32(load_act<TA>(a.dt_raw, ((size_t)b * T + c0 + row) * s.H + h) + dtb);
+            const float dt = row < Lc ? softplus_f32(dt_raw_next + dtb) : 0.f;
+            dt_raw_next = 0.f;
+            if (has_next && row < Ln) dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + c0 + Q + row) * s.H + h);
             float v = dt * A;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float o = __shfl_up_sync(0xffffffffu, v, off);
-                if ((tid & 31) >= off) v += o;
+                if (lane >= off) v += o;
             }
-            if ((tid & 31) == 31) sWsum[warp] = v;
+            if (lane == 31) sWsum[warp] = v;
             sDt[row] = dt;
             sS[row] = v;  // warp-local prefix for now
+        }
+        if (!tc::mbar_wait(bar_x, par)) {
+            atomicOr(a.err, ERR_MBAR_TIMEOUT_LOAD);
+            *sFlag = 1;
         }
         __syncthreads();
         if (half == 0) {
@@ -296,78 +329,79 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             for (int w = 0; w < (row >> 5); ++w) add += sWsum[w];
             sS[row] += add;
         }
-        __syncthreads();
-        const float Slast = sS[Lc - 1];
-        const float Si = sS[row];
-        const float wi = row < Lc ? expf(Slast - Si) * sDt[row] : 0.f;
-
-        // 3. conv + SiLU of this head's x channels for row i, columns of this half
-        float xf[PH];
-        {
-            const int t = c0 + row;
-#pragma unroll
-            for (int q8 = 0; q8 < PH / 8; ++q8) {
-                const int p0 = half * PH + q8 * 8;
-                float o[8];
-                if (row < Lc) {
-                    float acc[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[j] = sCb[p0 + j];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int tt = t - 3 + k;
-                        Act8<TA> v;
-                        bool have = true;
-                        if (tt >= 0)
-                            v.load(a.x, (((size_t)b * T + tt) * s.H + h) * P + p0);
-                        else if (a.init_conv)
-                            v.load(a.init_conv, ((size_t)b * (s.K - 1) + (s.K - 1 + tt)) * CH + (long)h * P + p0);
-                        else
-                            have = false;
-                        if (have) {
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) acc[j] = fmaf(sCw[(p0 + j) * 4 + k], v.get(j), acc[j]);
-                        }
-                    }
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) o[j] = silu_f32(acc[j]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) o[j] = 0.f;
-                }
-                uint32_t xh[4], wh[4], wl[4];
-#pragma unroll
-                for (int j = 0; j < 8; j += 2) {
-                    xf[q8 * 8 + j] = o[j];
-                    xf[q8 * 8 + j + 1] = o[j + 1];
-                    xh[j / 2] = pack2(o[j], o[j + 1]);
-                    const float w0 = wi * o[j], w1 = wi * o[j + 1];
-                    const uint32_t h0 = float_to_bf16_bits(w0), h1 = float_to_bf16_bits(w1);
-                    wh[j / 2] = h0 | (h1 << 16);
-                    wl[j / 2] = pack2(w0 - bf16_bits_to_float(h0), w1 - bf16_bits_to_float(h1));
-                }
-                const uint32_t off = tc::mn_inter_off(p0, row, P);
-                *reinterpret_cast<uint4*>(sm + L::kX + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
-                *reinterpret_cast<uint4*>(sm + L::kWh + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-                *reinterpret_cast<uint4*>(sm + L::kWl + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        if (c == 0 && a.init_conv) {
+            // frames -3..-1 (zero-filled by the copy) come from the initial conv tail
+            constexpr int V = L::kRowBytes / 16;
+            for (int e = tid; e < 3 * V; e += kSsdThreads) {
+                const int r = e / V, q = e % V;
+                *reinterpret_cast<uint4*>(sRaw + (size_t)r * L::kRowBytes + q * 16) =
+                    *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.init_conv) +
+                                                    (((size_t)b * 3 + r) * s.CH() + (size_t)h * P) * sizeof(TA) + q * 16);
             }
         }
+        __syncthreads();
+        if (*sFlag) { ok = false; break; }
+        const float Slast = sS[Lc - 1];
+        const float Si = sS[row];
+        const float wi = row < Lc ? __expf(Slast - Si) * sDt[row] : 0.f;
 
-        // 4. state: h_prev (bf16) into shared memory for Y_off, then h <- exp(S_last) h in TMEM
+        // 2. conv + SiLU of this head's x channels for row i (staged rows i..i+3)
+        float xf[PH];
+#pragma unroll
+        for (int q8 = 0; q8 < NQ; ++q8) {
+            const int p0 = half * PH + q8 * 8;
+            float o[8];
+            if (row < Lc) {
+                float acc[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = sCb[p0 + j];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    Act8<TA> v;
+                    v.load_rw(sRaw + (size_t)(row + k) * L::kRowBytes, p0);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[j] = fmaf(sCw[(p0 + j) * 4 + k], v.get(j), acc[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = silu_fast(acc[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = 0.f;
+            }
+            uint32_t xh[4], wh[4], wl[4];
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                xf[q8 * 8 + j] = o[j];
+                xf[q8 * 8 + j + 1] = o[j + 1];
+                xh[j / 2] = pack2(o[j], o[j + 1]);
+                const float w0 = wi * o[j], w1 = wi * o[j + 1];
+                const uint32_t h0 = float_to_bf16_bits(w0), h1 = float_to_bf16_bits(w1);
+                wh[j / 2] = h0 | (h1 << 16);
+                wl[j / 2] = pack2(w0 - bf16_bits_to_float(h0), w1 - bf16_bits_to_float(h1));
+            }
+            const uint32_t off = tc::mn_inter_off(p0, row, P);
+            *reinterpret_cast<uint4*>(sm + L::kX + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+            *reinterpret_cast<uint4*>(sm + L::kWh + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            *reinterpret_cast<uint4*>(sm + L::kWl + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        }
+
+        // 3. state: h_prev (bf16) into shared memory for Y_off, then h <- exp(S_last) h in TMEM
         {
-            const float decay = expf(Slast);
+            const float decay = __expf(Slast);
             const int n = row;
+            float v[NQ][8];
 #pragma unroll
-            for (int q8 = 0; q8 < PH / 8; ++q8) {
+            for (int q8 = 0; q8 < NQ; ++q8) tc::tmem_ld8(tm + lane_base + kColState + half * PH + q8 * 8, v[q8]);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int q8 = 0; q8 < NQ; ++q8) {
                 const int p0 = half * PH + q8 * 8;
-                float v[8];
-                tc::tmem_ld8(tm + lane_base + kColState + p0, v);
-                tc::tmem_wait_ld();
                 *reinterpret_cast<uint4*>(sm + L::kH + tc::mn_inter_off(p0, n, P)) =
-                    make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+                    make_uint4(pack2(v[q8][0], v[q8][1]), pack2(v[q8][2], v[q8][3]), pack2(v[q8][4], v[q8][5]),
+                               pack2(v[q8][6], v[q8][7]));
 #pragma unroll
-                for (int q = 0; q < 8; ++q) v[q] *= decay;
-                tc::tmem_st8(tm + lane_base + kColState + p0, v);
+                for (int q = 0; q < 8; ++q) v[q8][q] *= decay;
+                tc::tmem_st8(tm + lane_base + kColState + p0, v[q8]);
             }
             tc::tmem_wait_st();
         }
@@ -375,18 +409,20 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         tc::tc_fence_before();
         __syncthreads();
 
-        // 5. tensor-core phase 1: G, Y_off, state update
+        // 4. the staged x rows are consumed: stage the next chunk's while the tensor cores run
+        if (has_next && tid == 32) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, c0 + Q);
+
+        // 5. tensor-core phase 1: G = C~ B~^T (commit), the state terms that read
+        //    B~ lo (commit), then the rest of state += B~^T (w o x~)
         if (tid == 0) {
             tc::tc_fence_after();
-            if (!tc::mbar_wait(bar_ld, par)) {
+            if (!tc::mbar_wait(bar_a, par) || !tc::mbar_wait(bar_b, par)) {
                 atomicOr(a.err, ERR_MBAR_TIMEOUT_LOAD);
                 *sFlag = 1;
             } else {
                 const uint32_t sC = sbase + L::kC, sBh = sbase + L::kBh, sBl = sbase + L::kBl;
-                const uint32_t sX = sbase + L::kX, sWh = sbase + L::kWh, sWl = sbase + L::kWl, sH = sbase + L::kH;
-                (void)sX;
+                const uint32_t sWh = sbase + L::kWh, sWl = sbase + L::kWl;
                 const uint32_t idG = tc::idesc_bf16(128, 128, 0, 0);
-                const uint32_t idY = tc::idesc_bf16(128, P, 0, 1);
                 const uint32_t idS = tc::idesc_bf16(128, P, 1, 1);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -394,27 +430,21 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                     tc::mma_bf16(tm + kColG, tc::sdesc(sC + koff, 0, 1024, 2), tc::sdesc(sBh + koff, 0, 1024, 2), idG,
                                  ks > 0);
                 }
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
-                    tc::mma_bf16(tm + kColYo, tc::sdesc(sC + koff, 0, 1024, 2),
-                                 tc::sdesc(sH + ks * 2 * LBO_I, LBO_I, 128, 0), idY, ks > 0);
-                }
+                tc::mma_commit(bar_g);
+                for (int ks = 0; ks < ksteps; ++ks)
+                    tc::mma_bf16(tm + kColState, tc::sdesc(sBl + ks * 2048, kPanel, 1024, 2),
+                                 tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
+                tc::mma_commit(bar_bl);
                 for (int ks = 0; ks < ksteps; ++ks) {
                     const uint64_t dBh = tc::sdesc(sBh + ks * 2048, kPanel, 1024, 2);
-                    const uint64_t dBl = tc::sdesc(sBl + ks * 2048, kPanel, 1024, 2);
-                    const uint64_t dWh = tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0);
-                    const uint64_t dWl = tc::sdesc(sWl + ks * 2 * LBO_I, LBO_I, 128, 0);
-                    tc::mma_bf16(tm + kColState, dBh, dWh, idS, 1);
-                    tc::mma_bf16(tm + kColState, dBh, dWl, idS, 1);
-                    tc::mma_bf16(tm + kColState, dBl, dWh, idS, 1);
+                    tc::mma_bf16(tm + kColState, dBh, tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
+                    tc::mma_bf16(tm + kColState, dBh, tc::sdesc(sWl + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
                 }
-                tc::mma_commit(bar_m1);
             }
         }
         __syncthreads();
         if (*sFlag) { ok = false; break; }
-        if (!tc::mbar_wait(bar_m1, par)) {
+        if (!tc::mbar_wait(bar_g, par) || !tc::mbar_wait(bar_bl, par)) {
             atomicOr(a.err, ERR_MBAR_TIMEOUT_MMA);
             *sFlag = 1;
         }
@@ -422,66 +452,88 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         tc::tc_fence_after();
 
         // 6. M = G o exp(S_i - S_j) dt_j (j <= i) -> bf16, K-major SW128 over the B~ lo tile
+        //    (its readers are done; the remaining state MMAs run meanwhile)
         {
             const int i = row;
-#pragma unroll 1
-            for (int j0 = half * 64; j0 < half * 64 + 64; j0 += 16) {
-                float gv[16];
-                tc::tmem_ld16(tm + lane_base + kColG + j0, gv);
-                tc::tmem_wait_ld();
+            float gv[4][16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tc::tmem_ld16(tm + lane_base + kColG + half * 64 + q * 16, gv[q]);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j0 = half * 64 + q * 16;
                 uint32_t pk[8];
 #pragma unroll
-                for (int q = 0; q < 16; q += 2) {
+                for (int e = 0; e < 16; e += 2) {
+                    const int j = j0 + e;
                     float m0 = 0.f, m1 = 0.f;
-                    const int j = j0 + q;
-                    if (i < Lc && j <= i) m0 = gv[q] * expf(Si - sS[j]) * sDt[j];
-                    if (i < Lc && j + 1 <= i) m1 = gv[q + 1] * expf(Si - sS[j + 1]) * sDt[j + 1];
-                    pk[q / 2] = pack2(m0, m1);
+                    if (i < Lc && j <= i) m0 = gv[q][e] * __expf(Si - sS[j]) * sDt[j];
+                    if (i < Lc && j + 1 <= i) m1 = gv[q][e + 1] * __expf(Si - sS[j + 1]) * sDt[j + 1];
+                    pk[e / 2] = pack2(m0, m1);
                 }
                 *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0, kTR)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0 + 8, kTR)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0 + 8, kTR)) =
+                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
         }
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncthreads();
 
-        // 7. tensor-core phase 2: Y_diag = M x~
+        // 7. tensor-core phase 2: Y_diag = M x~ and Y_off = C~ h_prev^T
         if (tid == 0) {
             tc::tc_fence_after();
-            const uint32_t sM = sbase + L::kBl, sX = sbase + L::kX;
+            const uint32_t sM = sbase + L::kBl, sX = sbase + L::kX, sC = sbase + L::kC, sH = sbase + L::kH;
             const uint32_t idY = tc::idesc_bf16(128, P, 0, 1);
             for (int ks = 0; ks < ksteps; ++ks) {
                 const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
                 tc::mma_bf16(tm + kColYd, tc::sdesc(sM + koff, 0, 1024, 2), tc::sdesc(sX + ks * 2 * LBO_I, LBO_I, 128, 0),
                              idY, ks > 0);
             }
-            tc::mma_commit(bar_m2);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
+                tc::mma_bf16(tm + kColYo, tc::sdesc(sC + koff, 0, 1024, 2),
+                             tc::sdesc(sH + ks * 2 * LBO_I, LBO_I, 128, 0), idY, ks > 0);
+            }
+            tc::mma_commit(bar_y);
         }
         __syncwarp();
-        if (!tc::mbar_wait(bar_m2, par)) {
+        if (!tc::mbar_wait(bar_y, par)) {
             atomicOr(a.err, ERR_MBAR_TIMEOUT_MMA);
             *sFlag = 1;
         }
         if (__syncthreads_or(*sFlag)) { ok = false; break; }
         tc::tc_fence_after();
+        // every operand tile of this chunk is consumed: fetch the next chunk's
+        if (has_next && tid == 0) {
+            const uint8_t* src = tiles_of(c + 1);
+            tc::mbar_arrive_expect_tx(bar_a, 2 * kTileBytes);
+            tc::bulk_g2s(sm + L::kBh, src, kTileBytes, bar_a);
+            tc::bulk_g2s(sm + L::kC, src + 2 * kTileBytes, kTileBytes, bar_a);
+            tc::mbar_arrive_expect_tx(bar_b, kTileBytes);
+            tc::bulk_g2s(sm + L::kBl, src + kTileBytes, kTileBytes, bar_b);
+        }
 
         // 8. y = Y_diag + exp(S_i) Y_off + D x~. The TMEM loads are warp-collective
         //    (.sync.aligned): every lane issues them; only the stores are predicated.
         {
-            const float eS = expf(Si);
+            const float eS = __expf(Si);
             const bool live = row < Lc;
             const size_t ybase = (((size_t)b * T + c0 + row) * s.H + h) * P;
+            float yd[NQ][8], yo[NQ][8];
 #pragma unroll
-            for (int q8 = 0; q8 < PH / 8; ++q8) {
+            for (int q8 = 0; q8 < NQ; ++q8) {
+                tc::tmem_ld8(tm + lane_base + kColYd + half * PH + q8 * 8, yd[q8]);
+                tc::tmem_ld8(tm + lane_base + kColYo + half * PH + q8 * 8, yo[q8]);
+            }
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int q8 = 0; q8 < NQ; ++q8) {
                 const int p0 = half * PH + q8 * 8;
-                float yd[8], yo[8];
-                tc::tmem_ld8(tm + lane_base + kColYd + p0, yd);
-                tc::tmem_ld8(tm + lane_base + kColYo + p0, yo);
-                tc::tmem_wait_ld();
                 float out[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) out[q] = fmaf(eS, yo[q], yd[q]) + Dh * xf[q8 * 8 + q];
+                for (int q = 0; q < 8; ++q) out[q] = fmaf(eS, yo[q8][q], yd[q8][q]) + Dh * xf[q8 * 8 + q];
                 if (live) {
                     if constexpr (sizeof(TA) == 2) {
                         *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.y) + ybase + p0) =
@@ -500,22 +552,27 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         tc::tc_fence_after();
     }
 
+    pdl_trigger();
     // final state: TMEM [n][p] -> final_ssm [b,h,p,n]
     if (ok) {
         const int n = row;
-        for (int p0 = half * PH; p0 < (half + 1) * PH; p0 += 8) {
-            float v[8];
-            tc::tmem_ld8(tm + lane_base + kColState + p0, v);
-            tc::tmem_wait_ld();
-            if (n < s.N) {
+        float v[NQ][8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) a.final_ssm[(((size_t)b * s.H + h) * P + p0 + q) * s.N + n] = v[q];
-            }
+        for (int q8 = 0; q8 < NQ; ++q8) tc::tmem_ld8(tm + lane_base + kColState + half * PH + q8 * 8, v[q8]);
+        tc::tmem_wait_ld();
+        if (n < s.N) {
+#pragma unroll
+            for (int q8 = 0; q8 < NQ; ++q8)
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    a.final_ssm[(((size_t)b * s.H + h) * P + half * PH + q8 * 8 + q) * s.N + n] = v[q8][q];
         }
     } else if (tid == 0) {
-        // a wait gave up: let any bulk copy still in flight land before the CTA exits
-        tc::mbar_wait(bar_ld, 0, 100000000ull);
-        tc::mbar_wait(bar_ld, 1, 100000000ull);
+        // a wait gave up: let bulk copies still in flight land before the CTA exits
+        for (int i = 0; i < 3; ++i) {
+            tc::mbar_wait(bar_a + i, 0, 100000000ull);
+            tc::mbar_wait(bar_a + i, 1, 100000000ull);
+        }
     }
     // final conv tail (the last K-1 pre-conv frames). This CTA owns the tail of
     // its head's x channels (whose initial frames only it has read); the first
@@ -540,9 +597,50 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     if (warp == 0) tc::tmem_dealloc(tm, kTmemCols);
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, resolved once through the runtime.
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// x viewed as a 3-D tensor [b][T][H*P] (innermost last); a box is the
+// [kRawRows x P] pre-conv rows of one head for one chunk.
+template <typename TA, int P>
+cudaError_t make_x_map(const ScanArgs& a, CUtensorMap* map) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t HP = (cuuint64_t)a.s.H * P;
+    const cuuint64_t dims[3] = {HP, (cuuint64_t)a.T, (cuuint64_t)a.batch};
+    const cuuint64_t strides[2] = {HP * sizeof(TA), HP * (cuuint64_t)a.T * sizeof(TA)};
+    const cuuint32_t box[3] = {(cuuint32_t)P, (cuuint32_t)kRawRows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = sizeof(TA) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUresult r = enc(map, dt, 3, const_cast<void*>(a.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <typename TA, int P>
 cudaError_t launch_ssd(const ScanArgs& a, int nchunks, cudaStream_t st) {
-    const int smem = SsdSmem<P>::kBytes;
+    CUtensorMap tmx;
+    memset(&tmx, 0, sizeof(tmx));
+    if (nchunks > 0) {
+        cudaError_t me = make_x_map<TA, P>(a, &tmx);
+        if (me != cudaSuccess) return me;
+    }
+    const int smem = SsdSmem<TA, P>::kBytes;
     // once per process and instantiation (kept out of graph captures after the first call)
     static int configured_device = -1;
     int dev = 0;
@@ -553,16 +651,14 @@ cudaError_t launch_ssd(const ScanArgs& a, int nchunks, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    scan_ssd_kernel<TA, P><<<dim3(a.s.H, a.batch), kSsdThreads, smem, st>>>(a, nchunks);
-    return cudaGetLastError();
+    return launch_pdl(scan_ssd_kernel<TA, P>, dim3(a.s.H, a.batch), dim3(kSsdThreads), smem, st, a, nchunks, tmx);
 }
 
 template <typename TA>
 cudaError_t launch_bc_typed(const ScanArgs& a, cudaStream_t st) {
     const int nchunks = (a.T + a.chunk - 1) / a.chunk;
     if (nchunks == 0) return cudaSuccess;
-    scan_bc_kernel<TA><<<dim3(nchunks, a.s.G, a.batch), kBcThreads, 0, st>>>(a, nchunks);
-    return cudaGetLastError();
+    return launch_pdl(scan_bc_kernel<TA>, dim3(nchunks * 4, a.s.G, a.batch), dim3(kBcThreads), 0, st, a, nchunks);
 }
 
 template <typename TA>
@@ -574,7 +670,6 @@ cudaError_t launch_chunks_typed(const ScanArgs& a, cudaStream_t st) {
         case 48: return launch_ssd<TA, 48>(a, nchunks, st);
         case 64: return launch_ssd<TA, 64>(a, nchunks, st);
         case 80: return launch_ssd<TA, 80>(a, nchunks, st);
-        case 96: return launch_ssd<TA, 96>(a, nchunks, st);
         default: return cudaErrorInvalidValue;
     }
 }

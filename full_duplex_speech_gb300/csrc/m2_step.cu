@@ -12,6 +12,10 @@
 //     fp32 state update h <- exp(dt A) h + dt x (outer) B and y = h.C + D x.
 //     The state is 98% of the bytes; it is read and written once with 16-byte
 //     vector accesses, one row of N fp32 per N/4 lanes.
+// Both are launched with programmatic dependent launch: the conv kernel waits
+// for its predecessor before reading anything, then lets the state-update
+// kernel start, which issues its state loads (data written before the conv
+// kernel began) and only then waits for the conv kernel's outputs.
 #include "m2_common.cuh"
 #include "m2_launch.h"
 
@@ -19,7 +23,7 @@ namespace m2 {
 
 namespace {
 
-constexpr int kConvThreads = 256;
+constexpr int kConvThreads = 64;
 
 template <typename TA>
 __global__ void __launch_bounds__(kConvThreads) step_conv_kernel(StepArgs a) {
@@ -28,6 +32,8 @@ __global__ void __launch_bounds__(kConvThreads) step_conv_kernel(StepArgs a) {
     const long CH = s.CH(), HP = s.HP(), GN = s.GN();
     const long nvec = CH / 8;
     const long v = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    pdl_wait();     // inputs and the conv tail may come from the previous kernel
+    pdl_trigger();  // the state-update kernel may start loading the state
     if (v < nvec) {
         const long c = v * 8;
         // this frame's pre-conv input for channels [c, c+8)
@@ -98,6 +104,9 @@ __global__ void __launch_bounds__(kSsmThreads) step_ssm_kernel(StepArgs a) {
         prow[i] = (r < ROWS && p0 + r < s.P) ? p0 + r : -1;
         if (prow[i] >= 0) hv[i] = __ldcs(reinterpret_cast<const float4*>(state + (size_t)prow[i] * N + n4));
     }
+    // the state was written before the conv kernel started; its outputs are not
+    pdl_wait();
+    pdl_trigger();
     const float dt = a.ws_dt[(size_t)ses * s.H + h];
     const float A = -expf(__ldg(a.A_log + h));
     const float dA = expf(dt * A);
@@ -133,16 +142,14 @@ template <typename TA, int N>
 cudaError_t launch_ssm(const StepArgs& a, cudaStream_t st) {
     constexpr int ROWS = 16;
     dim3 grid((a.s.P + ROWS - 1) / ROWS, a.s.H, a.S);
-    step_ssm_kernel<TA, N, ROWS><<<grid, kSsmThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(step_ssm_kernel<TA, N, ROWS>, grid, dim3(kSsmThreads), 0, st, a);
 }
 
 template <typename TA>
 cudaError_t launch_typed(const StepArgs& a, cudaStream_t st) {
     const long nvec = a.s.CH() / 8 + a.s.H;
     dim3 g1((unsigned)((nvec + kConvThreads - 1) / kConvThreads), a.S);
-    step_conv_kernel<TA><<<g1, kConvThreads, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(step_conv_kernel<TA>, g1, dim3(kConvThreads), 0, st, a);
     if (e != cudaSuccess) return e;
     switch (a.s.N) {
         case 16: return launch_ssm<TA, 16>(a, st);

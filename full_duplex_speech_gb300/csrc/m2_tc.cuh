@@ -67,6 +67,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// 3-D tiled TMA load of one box of `tmap` at element coordinates (x, y, z)
+// (innermost first) into shared memory; out-of-range elements read as zero.
+// x * element size must be a multiple of 16 bytes; dst 128-byte aligned.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (tensor core, bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -46,7 +46,7 @@
  *           The activation dtype (x, B, C, dt_raw, y, conv tail) is
  *           m2_dims.act: bf16 or fp32.
  * Alignment. Every pointer must be 16-byte aligned (M2_EALIGN otherwise).
- * Shapes.   K == 4; N in {16, 32, 64, 128}; P a multiple of 16, at most 96;
+ * Shapes.   K == 4; N in {16, 32, 64, 128}; P a multiple of 16, at most 80;
  *           H a multiple of G; H*P and G*N multiples of 8. (The Nemotron-H
  *           mixer is H=128, P=80, N=128, G=8, K=4.) M2_ESHAPE otherwise.
  */

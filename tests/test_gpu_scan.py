@@ -88,7 +88,7 @@ def test_ragged_lengths(m2, T, chunk):
     check(m2, d, inp, chunk, 2, T)
 
 
-@pytest.mark.parametrize("shape", [Dims(H=6, P=48, N=32, G=3), Dims(H=4, P=96, N=128, G=1),
+@pytest.mark.parametrize("shape", [Dims(H=6, P=48, N=32, G=3), Dims(H=4, P=80, N=128, G=1),
                                    Dims(H=16, P=16, N=16, G=16)])
 def test_other_shapes(m2, shape):
     inp = mixer_inputs(31, shape, 3, 90, "f32")
