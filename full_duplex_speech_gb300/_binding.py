@@ -60,6 +60,10 @@ def load():
         lib.mamba2_step_workspace_bytes.restype = sz
         lib.mamba2_step.argtypes = [dp, ip] + [vp] * 13 + [sz, vp]
         lib.mamba2_step.restype = ip
+        lib.mamba2_step_noalloc.argtypes = [dp, ip] + [vp] * 12 + [vp]
+        lib.mamba2_step_noalloc.restype = ip
+        lib.mamba2_step_noalloc_max_bytes.argtypes = []
+        lib.mamba2_step_noalloc_max_bytes.restype = sz
         lib.mamba2_status_string.argtypes = [ip]
         lib.mamba2_status_string.restype = ctypes.c_char_p
         lib.mamba2_last_cuda_error.argtypes = []
@@ -164,4 +168,20 @@ def mamba2_step(d: M2Dims, n_sessions, x, B, C, dt_raw, A_log, D, dt_bias, conv_
         int(workspace_bytes), _stream(stream))
     if check and rc:
         raise M2Error(rc, "mamba2_step")
+    return rc
+
+
+def mamba2_step_noalloc_max_bytes() -> int:
+    return load().mamba2_step_noalloc_max_bytes()
+
+
+def mamba2_step_noalloc(d: M2Dims, n_sessions, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, ssm_state,
+                        conv_state, y, stream=None, check=True) -> int:
+    """mamba2_step with the library's fixed device scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    rc = load().mamba2_step_noalloc(
+        ctypes.byref(d), int(n_sessions), _p(x), _p(B), _p(C), _p(dt_raw), _p(A_log), _p(D),
+        _p(dt_bias), _p(conv_w), _p(conv_b), _p(ssm_state), _p(conv_state), _p(y), _stream(stream))
+    if check and rc:
+        raise M2Error(rc, "mamba2_step_noalloc")
     return rc

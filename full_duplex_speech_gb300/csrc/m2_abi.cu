@@ -72,6 +72,10 @@ m2::Shape shape_of(const m2_dims* d) {
 
 }  // namespace
 
+namespace m2 {
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+}  // namespace m2
+
 extern "C" {
 
 const char* mamba2_status_string(m2_status s) {

@@ -46,6 +46,9 @@ struct ScanArgs {
     unsigned int* err;  // device error word
 };
 
+// Records a CUDA error for mamba2_last_cuda_error() on the calling thread.
+void record_cuda_error(cudaError_t e);
+
 size_t scan_workspace_bytes(const Shape& s, int batch, int T, int chunk);
 // B/C conv prologue into the workspace tiles (first half of a scan).
 cudaError_t launch_scan_prepare(const ScanArgs& a, cudaStream_t st);

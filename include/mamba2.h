@@ -154,6 +154,33 @@ m2_status mamba2_step(const m2_dims* d, int n_sessions, const void* x, const voi
                       float* ssm_state, void* conv_state, void* y, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/* mamba2_step without a caller-provided workspace, for callers that cannot
+ * allocate device memory: a real-time frame loop that must not call
+ * cudaMalloc (it can synchronise the device mid-frame), a host that hands the
+ * library only tensors it already owns, or a binding without a device
+ * allocator. (This entry point has no counterpart in the VoiceChat pages; it
+ * is a property of this library.)
+ *
+ * The scratch is a fixed array inside the library's device image,
+ * mamba2_step_noalloc_max_bytes() bytes (1 MiB), present on every GPU that
+ * loads the library until the process exits. A request whose
+ * mamba2_step_workspace_bytes(d, n_sessions) exceeds it returns
+ * M2_EWORKSPACE before anything runs (at the Nemotron-H shape that is more
+ * than 21 sessions per call). The first call on a device looks up the
+ * array's device address (with that device current); make that first call
+ * before any stream capture. All calls share the one array: calls that may
+ * overlap on the GPU (on different streams, or from different host threads
+ * without ordering) race on it and give undefined results; calls ordered on
+ * one stream are safe. Nothing in it needs clearing between calls. Arguments,
+ * results and every other error are those of mamba2_step. */
+m2_status mamba2_step_noalloc(const m2_dims* d, int n_sessions, const void* x, const void* B,
+                              const void* C, const void* dt_raw, const float* A_log, const float* D,
+                              const float* dt_bias, const float* conv_w, const float* conv_b,
+                              float* ssm_state, void* conv_state, void* y, void* stream);
+
+/* Size in bytes of the fixed scratch used by mamba2_step_noalloc. */
+size_t mamba2_step_noalloc_max_bytes(void);
+
 /* Static description of a status code. */
 const char* mamba2_status_string(m2_status s);
 
