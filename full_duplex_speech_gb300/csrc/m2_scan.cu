@@ -161,6 +161,7 @@ __device__ void write_tail(const ScanArgs& a, int b, long c) {
 
 // ----------------------------------------------------------------- kernel 2
 constexpr int kSsdThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kRawRows = kTR + 3;  // pre-conv rows of one chunk plus the 3-frame halo
 // TMEM columns
 constexpr uint32_t kColG = 0, kColState = 128, kColYd = 256, kColYo = 384, kTmemCols = 512;
@@ -179,7 +180,8 @@ struct SsdSmem {
     static constexpr uint32_t kRowBytes = P * sizeof(TA);
     static constexpr uint32_t kS = kRaw + kRawRows * kRowBytes;  // float S[128]
     static constexpr uint32_t kDt = kS + 512;             // float dt[128]
-    static constexpr uint32_t kWsum = kDt + 512;          // float warp sums[8]
+    static constexpr uint32_t kTj = kDt + 512;            // float S_j log2e - log2(dt_j) [128]
+    static constexpr uint32_t kWsum = kTj + 512;          // float warp sums[8]
     static constexpr uint32_t kCw = kWsum + 64;           // float conv_w[P][4]
     static constexpr uint32_t kCb = kCw + P * 16;         // float conv_b[P]
     static constexpr uint32_t kBar = (kCb + P * 4 + 15) / 16 * 16;  // 6 mbarriers
@@ -188,8 +190,18 @@ struct SsdSmem {
     static constexpr uint32_t kBytes = kFlag + 4 + 1024;  // + slack to align the base to 1024
 };
 
+// Two fp32 -> packed bf16x2 (round to nearest even), a in the low half.
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
-    return (uint32_t)float_to_bf16_bits(a) | ((uint32_t)float_to_bf16_bits(b) << 16);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// 2^x on the special-function unit (ex2.approx: relative error ~2^-22, ftz).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 
 // Stages the pre-conv x rows of chunk c (frames c0-3 .. c0+kTR-1) of this head
@@ -224,6 +236,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
 
     float* sS = reinterpret_cast<float*>(sm + L::kS);
     float* sDt = reinterpret_cast<float*>(sm + L::kDt);
+    float* sTj = reinterpret_cast<float*>(sm + L::kTj);
     float* sWsum = reinterpret_cast<float*>(sm + L::kWsum);
     float* sCw = reinterpret_cast<float*>(sm + L::kCw);
     float* sCb = reinterpret_cast<float*>(sm + L::kCb);
@@ -247,8 +260,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         tc::tmem_relinquish();
     }
     for (int i = tid; i < P; i += kSsdThreads) {
-        const float4 wv = __ldg(reinterpret_cast<const float4*>(a.conv_w) + (long)h * P + i);
-        sCw[i * 4 + 0] = wv.x; sCw[i * 4 + 1] = wv.y; sCw[i * 4 + 2] = wv.z; sCw[i * 4 + 3] = wv.w;
+        reinterpret_cast<float4*>(sCw)[i] = __ldg(reinterpret_cast<const float4*>(a.conv_w) + (long)h * P + i);
         sCb[i] = __ldg(a.conv_b + (long)h * P + i);
     }
     const float A = -expf(__ldg(a.A_log + h));
@@ -343,6 +355,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         if (*sFlag) { ok = false; break; }
         const float Slast = sS[Lc - 1];
         const float Si = sS[row];
+        // column term of the decay mask in the log2 domain: M_ij = G_ij 2^(S_i log2e - T_j)
+        // with T_j = S_j log2e - log2(dt_j); +inf past the chunk end (dt_j = 0) gives 0
+        if (half == 0) sTj[row] = row < Lc ? fmaf(Si, kLog2e, -__log2f(sDt[row])) : __int_as_float(0x7f800000);
         const float wi = row < Lc ? __expf(Slast - Si) * sDt[row] : 0.f;
 
         // 2. conv + SiLU of this head's x channels for row i (staged rows i..i+3)
@@ -352,18 +367,21 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             const int p0 = half * PH + q8 * 8;
             float o[8];
             if (row < Lc) {
-                float acc[8];
+                Act8<TA> v[4];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[j] = sCb[p0 + j];
+                for (int k = 0; k < 4; ++k) v[k].load_rw(sRaw + (size_t)(row + k) * L::kRowBytes, p0);
+                const float4 b0 = reinterpret_cast<const float4*>(sCb + p0)[0];
+                const float4 b1 = reinterpret_cast<const float4*>(sCb + p0)[1];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    Act8<TA> v;
-                    v.load_rw(sRaw + (size_t)(row + k) * L::kRowBytes, p0);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[j] = fmaf(sCw[(p0 + j) * 4 + k], v.get(j), acc[j]);
+                for (int j = 0; j < 8; ++j) {
+                    const float4 w = reinterpret_cast<const float4*>(sCw)[p0 + j];
+                    float acc = j < 4 ? (&b0.x)[j] : (&b1.x)[j - 4];
+                    acc = fmaf(w.x, v[0].get(j), acc);
+                    acc = fmaf(w.y, v[1].get(j), acc);
+                    acc = fmaf(w.z, v[2].get(j), acc);
+                    acc = fmaf(w.w, v[3].get(j), acc);
+                    o[j] = silu_fast(acc);
                 }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = silu_fast(acc[j]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) o[j] = 0.f;
@@ -375,9 +393,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 xf[q8 * 8 + j + 1] = o[j + 1];
                 xh[j / 2] = pack2(o[j], o[j + 1]);
                 const float w0 = wi * o[j], w1 = wi * o[j + 1];
-                const uint32_t h0 = float_to_bf16_bits(w0), h1 = float_to_bf16_bits(w1);
-                wh[j / 2] = h0 | (h1 << 16);
-                wl[j / 2] = pack2(w0 - bf16_bits_to_float(h0), w1 - bf16_bits_to_float(h1));
+                const uint32_t hw = pack2(w0, w1);
+                wh[j / 2] = hw;
+                wl[j / 2] = pack2(w0 - __uint_as_float(hw << 16), w1 - __uint_as_float(hw & 0xFFFF0000u));
             }
             const uint32_t off = tc::mn_inter_off(p0, row, P);
             *reinterpret_cast<uint4*>(sm + L::kX + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
@@ -455,6 +473,8 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         //    (its readers are done; the remaining state MMAs run meanwhile)
         {
             const int i = row;
+            // rows past the chunk end: -inf makes every entry 0
+            const float si2 = i < Lc ? Si * kLog2e : __int_as_float(0xff800000);
             float gv[4][16];
 #pragma unroll
             for (int q = 0; q < 4; ++q) tc::tmem_ld16(tm + lane_base + kColG + half * 64 + q * 16, gv[q]);
@@ -464,12 +484,17 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 const int j0 = half * 64 + q * 16;
                 uint32_t pk[8];
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    const int j = j0 + e;
-                    float m0 = 0.f, m1 = 0.f;
-                    if (i < Lc && j <= i) m0 = gv[q][e] * __expf(Si - sS[j]) * sDt[j];
-                    if (i < Lc && j + 1 <= i) m1 = gv[q][e + 1] * __expf(Si - sS[j + 1]) * sDt[j + 1];
-                    pk[e / 2] = pack2(m0, m1);
+                for (int e4 = 0; e4 < 16; e4 += 4) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(sTj + j0 + e4);
+                    float m[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = j0 + e4 + e;
+                        const float v = gv[q][e4 + e] * ex2_approx(si2 - (&t4.x)[e]);
+                        m[e] = j <= i ? v : 0.f;
+                    }
+                    pk[e4 / 2] = pack2(m[0], m[1]);
+                    pk[e4 / 2 + 1] = pack2(m[2], m[3]);
                 }
                 *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0, kTR)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0 + 8, kTR)) =
