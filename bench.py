@@ -55,11 +55,26 @@ WORKLOAD = ("Nemotron-H Mamba2 mixer, real shape H=128 P=80 N=128 G=8 K=4, batch
 #   scan MMA flops per token (dense, chunk 128): C.B^T 2*Q*N*G + M.x 2*Q*P*H + state 2*N*P*H
 #   + C.h 2*N*P*H = 8,126,464.
 #   step bytes per session: 2 x 5,242,880 state + 2 x 73,728 conv tail + 24,832 in + 20,480 out.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one SSD-kernel
+# launch of this workload, from the ncu capture summarised in
+# profiles/scan_ssd_kernel_b1_T300.md. It describes one version of the kernel
+# source; for any other version the traffic is reported as unknown (null).
+SSD_TRAFFIC = {"bytes": 8875264, "m2_scan_cu_sha1": "4ecb90edd6913fb5da4da3f8b0605cd223c3e8fe"}
 SCAN_BYTES_PER_TOKEN = 45312
 STATE_BYTES = 128 * 80 * 128 * 4
 TAIL_BYTES = 3 * 12288 * 2
 SCAN_FLOPS_PER_TOKEN = 2 * CHUNK * 128 * 8 + 3 * (2 * 128 * 80 * 128)
 STEP_BYTES_PER_SESSION = 2 * STATE_BYTES + 2 * TAIL_BYTES + 24832 + 20480
+
+
+def ssd_traffic_for_current_source():
+    import hashlib
+    src = os.path.join(ROOT, "full_duplex_speech_gb300", "csrc", "m2_scan.cu")
+    try:
+        sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return SSD_TRAFFIC["bytes"] if sha == SSD_TRAFFIC["m2_scan_cu_sha1"] else None
 
 
 def load_peaks():
@@ -359,6 +374,7 @@ def run_gpu(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
+    torch.cuda.nvtx.range_push("bench_timed")
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(K // sweep):
@@ -366,6 +382,7 @@ def run_gpu(args, world, rank, local):
         if g_rem is not None:
             g_rem.replay()
         e1.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     t_wall1 = time.time()
     barrier(world)
@@ -403,12 +420,16 @@ def run_gpu(args, world, rank, local):
     # cached decode: one frame through all 27 layers (batch 1), and one layer
     # call for 64 sessions; graphs of consecutive step calls, no events between
     # them, so the launches keep their programmatic dependencies
+    torch.cuda.nvtx.range_push("step_frame")
     frame_us = _time_step_graph(m2, torch, stream, [(L.step_args()) for L in layers], reps=50)
+    torch.cuda.nvtx.range_pop()
     step_frame = {"us_per_frame_27_layers": frame_us, "us_per_layer": frame_us / N_LAYERS,
                   "achieved_gbs": N_LAYERS * STEP_BYTES_PER_SESSION / (frame_us * 1e-6) / 1e9}
     step_frame["frac_hbm"] = step_frame["achieved_gbs"] / peaks["hbm"]
     s64 = _sessions_step_args(m2, torch, dev, layers[0], 64)
+    torch.cuda.nvtx.range_push("step64")
     s64_us = _time_step_graph(m2, torch, stream, [s64], reps=50)
+    torch.cuda.nvtx.range_pop()
     step64 = {"sessions": 64, "us_per_call": s64_us,
               "achieved_gbs": 64 * STEP_BYTES_PER_SESSION / (s64_us * 1e-6) / 1e9}
     step64["frac_hbm"] = step64["achieved_gbs"] / peaks["hbm"]
@@ -464,7 +485,8 @@ def run_gpu(args, world, rank, local):
                        "l2": "inputs larger than L2: 27 layer buffer sets (~570 MB) cycled"},
             "roofline": {"bound": "hbm", "kernel": "scan_ssd_kernel (mamba2_scan_chunks)",
                          "achieved": ssd_gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                         "frac": ssd_gbs / peaks["hbm"], "traffic": args.ssd_traffic,
+                         "frac": ssd_gbs / peaks["hbm"],
+                         "traffic": args.ssd_traffic if args.ssd_traffic is not None else ssd_traffic_for_current_source(),
                          "algorithmic_bytes_per_launch": ssd_bytes, "avg_launch_ms": ssd_avg,
                          "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
                          "timing": timing_src},
