@@ -158,6 +158,13 @@ def barrier(world):
         dist.barrier()
 
 
+def aggregate(tokens_per_rank: float, ms_local: float, world: int, device=None):
+    """Whole-job throughput: tokens of all ranks over the slowest rank's time
+    (independent replicas, weak scaling). Returns (tokens/s, max ms)."""
+    ms = reduce_max(ms_local, world, device)
+    return world * tokens_per_rank / (ms * 1e-3), ms
+
+
 def reduce_max(x: float, world: int, device=None) -> float:
     """Max of a float over all ranks (the only cross-rank operation)."""
     if world == 1:
@@ -389,7 +396,7 @@ def run_gpu(args, world, rank, local):
     time.sleep(0.2)
     clocks.stop()
     ms_local = e0.elapsed_time(e1)
-    ms_total = reduce_max(ms_local, world, dev)
+    value, ms_total = aggregate(K * (T_FRAMES + 1), ms_local, world, dev)
     ms_per_step = ms_total / K
 
     # per-kernel durations: from the events inside the last full sweep of the timed region
@@ -475,7 +482,6 @@ def run_gpu(args, world, rank, local):
                           f"scaled by 128/{info['heads']}")}
 
     if rank == 0:
-        value = world * (T_FRAMES + 1) / (ms_per_step * 1e-3)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

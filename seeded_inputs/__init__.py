@@ -179,3 +179,31 @@ def ssm_state_inputs(seed: int, d: Dims, batch: int, scale: float = 0.05) -> np.
     """A random fp32 SSM state [b, H, P, N] for continuation tests."""
     rng = np.random.default_rng([seed, 0x5EED, 4])
     return (scale * rng.standard_normal((batch, d.H, d.P, d.N))).astype(np.float32)
+
+
+def device_mixer_inputs(seed: int, d: Dims, batch: int, T: int, device, act: str = "bf16") -> dict:
+    """The same distributions drawn on a device with torch's generator, for
+    workloads too large to draw on the host (the long-prefill run: 27 layers
+    x 4 x 4096 frames). Returns torch tensors (activations in the act dtype,
+    parameters fp32). Consumers that need host copies slice and copy them."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + 17)
+    dt = torch.bfloat16 if act == "bf16" else torch.float32
+
+    def normal(shape, sigma=1.0):
+        return (torch.randn(shape, generator=g, device=device) * sigma).to(dt)
+
+    def uniform(shape, lo, hi):
+        return torch.rand(shape, generator=g, device=device, dtype=torch.float64) * (hi - lo) + lo
+
+    out = dict(x=normal((batch, T, d.H, d.P)), B=normal((batch, T, d.G, d.N)), C=normal((batch, T, d.G, d.N)),
+               dt_raw=normal((batch, T, d.H), 0.5))
+    dt_target = torch.exp(uniform((d.H,), np.log(1e-3), np.log(0.1)))
+    out["dt_bias"] = torch.log(torch.expm1(dt_target)).float()
+    out["A_log"] = torch.log(uniform((d.H,), 1.0, 16.0)).float()
+    out["D"] = torch.randn((d.H,), generator=g, device=device, dtype=torch.float64).float()
+    out["conv_w"] = uniform((d.CH, d.K), -0.5, 0.5).float().contiguous()
+    out["conv_b"] = uniform((d.CH,), -0.5, 0.5).float()
+    out["act"] = act
+    return out
