@@ -289,9 +289,70 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     }
     // first chunk's pre-conv x rows and dt_raw (inputs written before the prologue kernel)
     if (nchunks > 0 && tid == 32) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, 0);
+    // dt_raw of this thread's row, loaded one chunk ahead of the dt phase that uses it
     float dt_raw_next = 0.f;
     if (nchunks > 0 && half == 0 && row < min(Q, T))
         dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + row) * s.H + h);
+
+    // dt = softplus(dt_raw + dt_bias), a = dt A, inclusive cumulative sum S over
+    // a chunk of Lx rows, and the decay-mask column term in the log2 domain,
+    // T_j = S_j log2e - log2(dt_j) (+inf past the chunk end: dt_j = 0), all into
+    // shared memory. Every thread must call it (it holds a barrier).
+    auto dt_phase = [&](int Lx, float raw) {
+        float v = 0.f, dt = 0.f;
+        if (half == 0) {
+            dt = row < Lx ? softplus_f32(raw + dtb) : 0.f;
+            v = dt * A;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += o;
+            }
+            if (lane == 31) sWsum[warp] = v;
+        }
+        __syncthreads();
+        if (half == 0) {
+            float add = 0.f;
+            for (int w = 0; w < (row >> 5); ++w) add += sWsum[w];
+            const float S = v + add;
+            sS[row] = S;
+            sDt[row] = dt;
+            sTj[row] = row < Lx ? fmaf(S, kLog2e, -__log2f(dt)) : __int_as_float(0x7f800000);
+        }
+    };
+
+    // y = (D x~ + M x~) + exp(S_i) Y_off for the chunk whose results sit in TMEM.
+    // The TMEM loads are warp-collective (.sync.aligned): every lane issues
+    // them; only the stores are predicated.
+    auto y_epilogue = [&](int c0y, int Ly, float eSy) {
+        const bool live = row < Ly;
+        const size_t ybase = (((size_t)b * T + c0y + row) * s.H + h) * P;
+        float yd[NQ][8], yo[NQ][8];
+#pragma unroll
+        for (int q8 = 0; q8 < NQ; ++q8) {
+            tc::tmem_ld8(tm + lane_base + kColYd + half * PH + q8 * 8, yd[q8]);
+            tc::tmem_ld8(tm + lane_base + kColYo + half * PH + q8 * 8, yo[q8]);
+        }
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int q8 = 0; q8 < NQ; ++q8) {
+            const int p0 = half * PH + q8 * 8;
+            float out[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) out[q] = fmaf(eSy, yo[q8][q], yd[q8][q]);
+            if (live) {
+                if constexpr (sizeof(TA) == 2) {
+                    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.y) + ybase + p0) =
+                        make_uint4(pack2(out[0], out[1]), pack2(out[2], out[3]), pack2(out[4], out[5]),
+                                   pack2(out[6], out[7]));
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + ybase + p0);
+                    dst[0] = make_float4(out[0], out[1], out[2], out[3]);
+                    dst[1] = make_float4(out[4], out[5], out[6], out[7]);
+                }
+            }
+        }
+    };
 
     const uint32_t sbase = tc::smem_u32(sm);
     const uint8_t* ws = reinterpret_cast<const uint8_t*>(a.ws);
@@ -307,7 +368,18 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         tc::mbar_arrive_expect_tx(bar_b, kTileBytes);
         tc::bulk_g2s(sm + L::kBl, src + kTileBytes, kTileBytes, bar_b);
     }
+    if (nchunks > 0) {
+        dt_phase(min(Q, T), dt_raw_next);
+        dt_raw_next = 0.f;
+        if (half == 0 && nchunks > 1 && row < min(Q, T - Q))
+            dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + Q + row) * s.H + h);
+    }
 
+    // The chunk loop is skewed so that CUDA-core work overlaps the tensor cores:
+    // the y epilogue of chunk c-1 runs under chunk c's phase-1 MMAs, and the dt
+    // phase of chunk c+1 under chunk c's phase-2 MMAs.
+    float eS_prev = 0.f;
+    int L_prev = 0, c0_prev = 0;
     for (int c = 0; c < nchunks; ++c) {
         const int c0 = c * Q;
         const int Lc = min(Q, T - c0);
@@ -315,32 +387,14 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         const uint32_t par = c & 1;
         const bool has_next = c + 1 < nchunks;
         const int Ln = has_next ? min(Q, T - c0 - Q) : 0;
+        const int Lnn = c + 2 < nchunks ? min(Q, T - c0 - 2 * Q) : 0;
 
-        // 1. dt = softplus(dt_raw + dt_bias), a = dt A, inclusive cumulative sum S
-        if (half == 0) {
-            const float dt = row < Lc ? softplus_f32(dt_raw_next + dtb) : 0.f;
-            dt_raw_next = 0.f;
-            if (has_next && row < Ln) dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + c0 + Q + row) * s.H + h);
-            float v = dt * A;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, v, off);
-                if (lane >= off) v += o;
-            }
-            if (lane == 31) sWsum[warp] = v;
-            sDt[row] = dt;
-            sS[row] = v;  // warp-local prefix for now
-        }
+        // 1. this chunk's staged x rows (and its dt phase, done one step earlier)
         if (!tc::mbar_wait(bar_x, par)) {
             atomicOr(a.err, ERR_MBAR_TIMEOUT_LOAD);
             *sFlag = 1;
         }
         __syncthreads();
-        if (half == 0) {
-            float add = 0.f;
-            for (int w = 0; w < (row >> 5); ++w) add += sWsum[w];
-            sS[row] += add;
-        }
         if (c == 0 && a.init_conv) {
             // frames -3..-1 (zero-filled by the copy) come from the initial conv tail
             constexpr int V = L::kRowBytes / 16;
@@ -350,14 +404,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                     *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.init_conv) +
                                                     (((size_t)b * 3 + r) * s.CH() + (size_t)h * P) * sizeof(TA) + q * 16);
             }
+            __syncthreads();
         }
-        __syncthreads();
         if (*sFlag) { ok = false; break; }
         const float Slast = sS[Lc - 1];
         const float Si = sS[row];
-        // column term of the decay mask in the log2 domain: M_ij = G_ij 2^(S_i log2e - T_j)
-        // with T_j = S_j log2e - log2(dt_j); +inf past the chunk end (dt_j = 0) gives 0
-        if (half == 0) sTj[row] = row < Lc ? fmaf(Si, kLog2e, -__log2f(sDt[row])) : __int_as_float(0x7f800000);
         const float wi = row < Lc ? __expf(Slast - Si) * sDt[row] : 0.f;
 
         // 2. conv + SiLU of this head's x channels for row i (staged rows i..i+3)
@@ -460,6 +511,21 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 }
             }
         }
+
+        // 6. meanwhile: the previous chunk's y (phase 1 touches only the G and
+        //    state columns), then this chunk's D x~ preloaded into the Y_diag
+        //    accumulator that phase 2 adds M x~ onto
+        if (c > 0) y_epilogue(c0_prev, L_prev, eS_prev);
+        {
+            float dx[8];
+#pragma unroll
+            for (int q8 = 0; q8 < NQ; ++q8) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) dx[q] = Dh * xf[q8 * 8 + q];
+                tc::tmem_st8(tm + lane_base + kColYd + half * PH + q8 * 8, dx);
+            }
+            tc::tmem_wait_st();
+        }
         __syncthreads();
         if (*sFlag) { ok = false; break; }
         if (!tc::mbar_wait(bar_g, par) || !tc::mbar_wait(bar_bl, par)) {
@@ -469,7 +535,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         if (__syncthreads_or(*sFlag)) { ok = false; break; }
         tc::tc_fence_after();
 
-        // 6. M = G o exp(S_i - S_j) dt_j (j <= i) -> bf16, K-major SW128 over the B~ lo tile
+        // 7. M = G o exp(S_i - S_j) dt_j (j <= i) -> bf16, K-major SW128 over the B~ lo tile
         //    (its readers are done; the remaining state MMAs run meanwhile)
         {
             const int i = row;
@@ -505,7 +571,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         tc::tc_fence_before();
         __syncthreads();
 
-        // 7. tensor-core phase 2: Y_diag = M x~ and Y_off = C~ h_prev^T
+        // 8. tensor-core phase 2: Y_diag += M x~ (onto D x~) and Y_off = C~ h_prev^T
         if (tid == 0) {
             tc::tc_fence_after();
             const uint32_t sM = sbase + L::kBl, sX = sbase + L::kX, sC = sbase + L::kC, sH = sbase + L::kH;
@@ -513,7 +579,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             for (int ks = 0; ks < ksteps; ++ks) {
                 const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
                 tc::mma_bf16(tm + kColYd, tc::sdesc(sM + koff, 0, 1024, 2), tc::sdesc(sX + ks * 2 * LBO_I, LBO_I, 128, 0),
-                             idY, ks > 0);
+                             idY, 1);
             }
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -523,7 +589,15 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             }
             tc::mma_commit(bar_y);
         }
-        __syncwarp();
+
+        // 9. meanwhile: the next chunk's dt phase (the mask above was the last
+        //    reader of this chunk's S, dt and T_j; S_i is kept in a register)
+        if (has_next) {
+            dt_phase(Ln, dt_raw_next);
+            dt_raw_next = 0.f;
+            if (half == 0 && row < Lnn)
+                dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + c0 + 2 * Q + row) * s.H + h);
+        }
         if (!tc::mbar_wait(bar_y, par)) {
             atomicOr(a.err, ERR_MBAR_TIMEOUT_MMA);
             *sFlag = 1;
@@ -539,43 +613,12 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             tc::mbar_arrive_expect_tx(bar_b, kTileBytes);
             tc::bulk_g2s(sm + L::kBl, src + kTileBytes, kTileBytes, bar_b);
         }
-
-        // 8. y = Y_diag + exp(S_i) Y_off + D x~. The TMEM loads are warp-collective
-        //    (.sync.aligned): every lane issues them; only the stores are predicated.
-        {
-            const float eS = __expf(Si);
-            const bool live = row < Lc;
-            const size_t ybase = (((size_t)b * T + c0 + row) * s.H + h) * P;
-            float yd[NQ][8], yo[NQ][8];
-#pragma unroll
-            for (int q8 = 0; q8 < NQ; ++q8) {
-                tc::tmem_ld8(tm + lane_base + kColYd + half * PH + q8 * 8, yd[q8]);
-                tc::tmem_ld8(tm + lane_base + kColYo + half * PH + q8 * 8, yo[q8]);
-            }
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int q8 = 0; q8 < NQ; ++q8) {
-                const int p0 = half * PH + q8 * 8;
-                float out[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) out[q] = fmaf(eS, yo[q8][q], yd[q8][q]) + Dh * xf[q8 * 8 + q];
-                if (live) {
-                    if constexpr (sizeof(TA) == 2) {
-                        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.y) + ybase + p0) =
-                            make_uint4(pack2(out[0], out[1]), pack2(out[2], out[3]), pack2(out[4], out[5]),
-                                       pack2(out[6], out[7]));
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + ybase + p0);
-                        dst[0] = make_float4(out[0], out[1], out[2], out[3]);
-                        dst[1] = make_float4(out[4], out[5], out[6], out[7]);
-                    }
-                }
-            }
-        }
-        tc::tc_fence_before();
-        __syncthreads();
-        tc::tc_fence_after();
+        eS_prev = __expf(Si);
+        L_prev = Lc;
+        c0_prev = c0;
     }
+    // the last chunk's y
+    if (ok && nchunks > 0) y_epilogue(c0_prev, L_prev, eS_prev);
 
     pdl_trigger();
     // final state: TMEM [n][p] -> final_ssm [b,h,p,n]
