@@ -278,17 +278,20 @@ class Layer:
 
 
 def enqueue_step(m2, L, stream, ev=None):
-    """One bench step on `stream`: scan (prologue + SSD kernel) then one cached step.
-    ev = (a, b, c) events around the SSD kernel and the step call."""
+    """One bench step on `stream`: the scan, then one cached step. Without
+    events it is the public calls (mamba2_conv_scan, mamba2_step). With
+    ev = (a, b, c) the scan is issued as its two halves with events around
+    the SSD kernel (mamba2_scan_chunks) and around the step call."""
+    if not ev:
+        m2.mamba2_conv_scan(*L.scan_args(), stream=stream)
+        m2.mamba2_step(*L.step_args(), stream=stream)
+        return
     m2.mamba2_scan_prepare_bc(*L.scan_args(), stream=stream)
-    if ev:
-        ev[0].record(stream)
+    ev[0].record(stream)
     m2.mamba2_scan_chunks(*L.scan_args(), stream=stream)
-    if ev:
-        ev[1].record(stream)
+    ev[1].record(stream)
     m2.mamba2_step(*L.step_args(), stream=stream)
-    if ev:
-        ev[2].record(stream)
+    ev[2].record(stream)
 
 
 def _time_step_graph(m2, torch, stream, arg_list, reps):
@@ -357,12 +360,20 @@ def run_gpu(args, world, rank, local):
         graph_events = False
 
     sweep = min(K, N_LAYERS)
-    evs = [[torch.cuda.Event(enable_timing=True, external=True) if graph_events else None for _ in range(3)]
-           for _ in range(sweep)]
     g_full = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_full, stream=stream):
         for i in range(sweep):
-            enqueue_step(m2, layers[i], stream, evs[i] if graph_events else None)
+            enqueue_step(m2, layers[i], stream)
+    # a second graph of one sweep with events around the SSD kernel and the step
+    # call, replayed right after the timed region for per-kernel durations
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) if graph_events else None for _ in range(3)]
+           for _ in range(N_LAYERS)]
+    g_ev = None
+    if graph_events:
+        g_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_ev, stream=stream):
+            for i in range(N_LAYERS):
+                enqueue_step(m2, layers[i], stream, evs[i])
     rem = K % sweep
     g_rem = None
     if rem:
@@ -392,6 +403,11 @@ def run_gpu(args, world, rank, local):
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     t_wall1 = time.time()
+    if g_ev is not None:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g_ev.replay()
+        torch.cuda.synchronize()
     barrier(world)
     time.sleep(0.2)
     clocks.stop()
@@ -401,19 +417,20 @@ def run_gpu(args, world, rank, local):
 
     # per-kernel durations: from the events inside the last full sweep of the timed region
     if graph_events:
-        ssd_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(sweep)]
-        step_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(sweep)]
-        timing_src = "CUDA events captured in the replayed graph (last timed sweep)"
+        ssd_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(N_LAYERS)]
+        step_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(N_LAYERS)]
+        timing_src = ("CUDA events in a graph of one 27-layer sweep (scan issued as its two halves), "
+                      "replayed right after the timed region")
     else:
         ssd_ms, step_ms = [], []
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(sweep)]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(N_LAYERS)]
         with torch.cuda.stream(stream):
             torch.cuda._sleep(50_000_000)  # keep the GPU busy while the host enqueues ahead
-            for i in range(sweep):
+            for i in range(N_LAYERS):
                 enqueue_step(m2, layers[i], stream, ev[i])
         torch.cuda.synchronize()
-        ssd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(sweep)]
-        step_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(sweep)]
+        ssd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(N_LAYERS)]
+        step_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(N_LAYERS)]
         timing_src = "CUDA events on the launch stream (eager, host ahead of the GPU)"
     ssd_avg = sum(ssd_ms) / len(ssd_ms)
     step_avg = sum(step_ms) / len(step_ms)

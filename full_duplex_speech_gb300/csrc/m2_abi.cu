@@ -243,7 +243,7 @@ m2_status mamba2_scan_chunks(M2_SCAN_PARAMS) {
     m2::ScanArgs a;
     m2_status st = scan_setup(M2_SCAN_ARGS, &a);
     if (st != M2_OK || d->batch == 0) return st;
-    cudaError_t e = m2::launch_scan_chunks(a, static_cast<cudaStream_t>(stream));
+    cudaError_t e = m2::launch_scan_chunks(a, false, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M2_OK : cuda_fail(e);
 }
 
@@ -252,7 +252,7 @@ m2_status mamba2_conv_scan(M2_SCAN_PARAMS) {
     m2_status st = scan_setup(M2_SCAN_ARGS, &a);
     if (st != M2_OK || d->batch == 0) return st;
     cudaError_t e = m2::launch_scan_prepare(a, static_cast<cudaStream_t>(stream));
-    if (e == cudaSuccess) e = m2::launch_scan_chunks(a, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = m2::launch_scan_chunks(a, true, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M2_OK : cuda_fail(e);
 }
 

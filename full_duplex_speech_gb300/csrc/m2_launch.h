@@ -53,6 +53,8 @@ size_t scan_workspace_bytes(const Shape& s, int batch, int T, int chunk);
 // B/C conv prologue into the workspace tiles (first half of a scan).
 cudaError_t launch_scan_prepare(const ScanArgs& a, cudaStream_t st);
 // Fused chunked SSD over prepared tiles, final state and conv tail (second half).
-cudaError_t launch_scan_chunks(const ScanArgs& a, cudaStream_t st);
+// after_prologue: the launch directly follows launch_scan_prepare of the same
+// call on the stream (allows an early, programmatically dependent start).
+cudaError_t launch_scan_chunks(const ScanArgs& a, bool after_prologue, cudaStream_t st);
 
 }  // namespace m2

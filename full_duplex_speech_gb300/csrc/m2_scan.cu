@@ -160,7 +160,13 @@ __device__ void write_tail(const ScanArgs& a, int b, long c) {
 }
 
 // ----------------------------------------------------------------- kernel 2
-constexpr int kSsdThreads = 256;
+// Eight compute warps (two per TMEM lane quarter, each taking half of the P
+// columns) and one control warp whose elected thread issues every TMA copy
+// and tcgen05 instruction. The issuing thread stalls while the tensor cores
+// work through its MMAs, so it is kept out of the CUDA-core phases.
+constexpr int kComputeThreads = 256;
+constexpr int kSsdThreads = kComputeThreads + 32;
+constexpr int kCtrl = kComputeThreads;  // the control thread
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kRawRows = kTR + 3;  // pre-conv rows of one chunk plus the 3-frame halo
 // TMEM columns
@@ -184,8 +190,8 @@ struct SsdSmem {
     static constexpr uint32_t kWsum = kTj + 512;          // float warp sums[8]
     static constexpr uint32_t kCw = kWsum + 64;           // float conv_w[P][4]
     static constexpr uint32_t kCb = kCw + P * 16;         // float conv_b[P]
-    static constexpr uint32_t kBar = (kCb + P * 4 + 15) / 16 * 16;  // 6 mbarriers
-    static constexpr uint32_t kTmem = kBar + 48;          // TMEM base address
+    static constexpr uint32_t kBar = (kCb + P * 4 + 15) / 16 * 16;  // 8 mbarriers
+    static constexpr uint32_t kTmem = kBar + 64;          // TMEM base address
     static constexpr uint32_t kFlag = kTmem + 4;          // abort flag
     static constexpr uint32_t kBytes = kFlag + 4 + 1024;  // + slack to align the base to 1024
 };
@@ -204,6 +210,9 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return r;
 }
 
+// Barrier among the eight compute warps only (the control warp never joins).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
 // Stages the pre-conv x rows of chunk c (frames c0-3 .. c0+kTR-1) of this head
 // into shared memory with one 3-D TMA box copy of [kRawRows frames x P
 // channels]; frames outside [0, T) read as zero (the caller patches the three
@@ -220,7 +229,7 @@ template <typename TA, int P>
 __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, int nchunks,
                                                                   const __grid_constant__ CUtensorMap tmx) {
     using L = SsdSmem<TA, P>;
-    constexpr int PH = P / 2;   // columns handled by each half of the CTA
+    constexpr int PH = P / 2;   // columns handled by each half of the compute warps
     constexpr int NQ = PH / 8;  // 8-column groups per half
     constexpr uint32_t LBO_I = (P / 8) * 128;  // K-group stride of the interleaved tiles
     extern __shared__ uint8_t smem_raw[];
@@ -231,7 +240,8 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     const int g = h / (s.H / s.G);
     const int T = a.T, Q = a.chunk;
     const long HP = s.HP();
-    const int tid = threadIdx.x, row = tid & 127, half = tid >> 7, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, row = tid & 127, half = (tid >> 7) & 1, warp = tid >> 5, lane = tid & 31;
+    const bool compute = tid < kComputeThreads;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     float* sS = reinterpret_cast<float*>(sm + L::kS);
@@ -241,21 +251,35 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     float* sCw = reinterpret_cast<float*>(sm + L::kCw);
     float* sCb = reinterpret_cast<float*>(sm + L::kCb);
     uint8_t* sRaw = sm + L::kRaw;
-    uint64_t* bar_a = reinterpret_cast<uint64_t*>(sm + L::kBar);  // C~ hi + B~ hi tiles
-    uint64_t* bar_b = bar_a + 1;                                   // B~ lo tile
-    uint64_t* bar_x = bar_a + 2;                                   // pre-conv x rows
+    uint64_t* bar_a = reinterpret_cast<uint64_t*>(sm + L::kBar);  // C~ hi + B~ hi tiles landed
+    uint64_t* bar_b = bar_a + 1;                                   // B~ lo tile landed
+    uint64_t* bar_x = bar_a + 2;                                   // pre-conv x rows landed
     uint64_t* bar_g = bar_a + 3;                                   // G done
     uint64_t* bar_bl = bar_a + 4;                                  // state terms reading B~ lo done
     uint64_t* bar_y = bar_a + 5;                                   // every MMA of the chunk done
+    uint64_t* bar_op1 = bar_a + 6;                                 // phase-1 operands written (256 arrivals)
+    uint64_t* bar_op2 = bar_a + 7;                                 // phase-2 operands written (256 arrivals)
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::kTmem);
     volatile uint32_t* sFlag = reinterpret_cast<uint32_t*>(sm + L::kFlag);
 
-    if (tid == 0) {
+    // Bounded wait that gives up at once after any earlier timeout in the CTA,
+    // so a failure cannot turn into a hang; it records `code` when it runs out.
+    auto wait_ok = [&](uint64_t* bar, uint32_t parity, unsigned code) -> bool {
+        if (*sFlag) return false;
+        if (tc::mbar_wait(bar, parity)) return true;
+        atomicOr(a.err, code);
+        *sFlag = 1;
+        return false;
+    };
+
+    if (tid == kCtrl) {
         for (int i = 0; i < 6; ++i) tc::mbar_init(bar_a + i, 1);
+        tc::mbar_init(bar_op1, kComputeThreads);
+        tc::mbar_init(bar_op2, kComputeThreads);
         tc::fence_mbar_init();
         *sFlag = 0;
     }
-    if (warp == 0) {
+    if (!compute) {
         tc::tmem_alloc(sTmem, kTmemCols);
         tc::tmem_relinquish();
     }
@@ -271,358 +295,362 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     tc::tc_fence_after();
     const uint32_t tm = *sTmem;
 
-    // initial state -> TMEM [n lanes][p columns]; rows n >= N stay zero
-    {
-        const int n = row;
-#pragma unroll
-        for (int q8 = 0; q8 < NQ; ++q8) {
-            const int p0 = half * PH + q8 * 8;
-            float v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                v[q] = (a.init_ssm && n < s.N)
-                           ? __ldg(a.init_ssm + (((size_t)b * s.H + h) * P + p0 + q) * s.N + n)
-                           : 0.f;
-            tc::tmem_st8(tm + lane_base + kColState + p0, v);
-        }
-        tc::tmem_wait_st();
-    }
-    // first chunk's pre-conv x rows and dt_raw (inputs written before the prologue kernel)
-    if (nchunks > 0 && tid == 32) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, 0);
-    // dt_raw of this thread's row, loaded one chunk ahead of the dt phase that uses it
-    float dt_raw_next = 0.f;
-    if (nchunks > 0 && half == 0 && row < min(Q, T))
-        dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + row) * s.H + h);
-
-    // dt = softplus(dt_raw + dt_bias), a = dt A, inclusive cumulative sum S over
-    // a chunk of Lx rows, and the decay-mask column term in the log2 domain,
-    // T_j = S_j log2e - log2(dt_j) (+inf past the chunk end: dt_j = 0), all into
-    // shared memory. Every thread must call it (it holds a barrier).
-    auto dt_phase = [&](int Lx, float raw) {
-        float v = 0.f, dt = 0.f;
-        if (half == 0) {
-            dt = row < Lx ? softplus_f32(raw + dtb) : 0.f;
-            v = dt * A;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, v, off);
-                if (lane >= off) v += o;
-            }
-            if (lane == 31) sWsum[warp] = v;
-        }
-        __syncthreads();
-        if (half == 0) {
-            float add = 0.f;
-            for (int w = 0; w < (row >> 5); ++w) add += sWsum[w];
-            const float S = v + add;
-            sS[row] = S;
-            sDt[row] = dt;
-            sTj[row] = row < Lx ? fmaf(S, kLog2e, -__log2f(dt)) : __int_as_float(0x7f800000);
-        }
-    };
-
-    // y = (D x~ + M x~) + exp(S_i) Y_off for the chunk whose results sit in TMEM.
-    // The TMEM loads are warp-collective (.sync.aligned): every lane issues
-    // them; only the stores are predicated.
-    auto y_epilogue = [&](int c0y, int Ly, float eSy) {
-        const bool live = row < Ly;
-        const size_t ybase = (((size_t)b * T + c0y + row) * s.H + h) * P;
-        float yd[NQ][8], yo[NQ][8];
-#pragma unroll
-        for (int q8 = 0; q8 < NQ; ++q8) {
-            tc::tmem_ld8(tm + lane_base + kColYd + half * PH + q8 * 8, yd[q8]);
-            tc::tmem_ld8(tm + lane_base + kColYo + half * PH + q8 * 8, yo[q8]);
-        }
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int q8 = 0; q8 < NQ; ++q8) {
-            const int p0 = half * PH + q8 * 8;
-            float out[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) out[q] = fmaf(eSy, yo[q8][q], yd[q8][q]);
-            if (live) {
-                if constexpr (sizeof(TA) == 2) {
-                    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.y) + ybase + p0) =
-                        make_uint4(pack2(out[0], out[1]), pack2(out[2], out[3]), pack2(out[4], out[5]),
-                                   pack2(out[6], out[7]));
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + ybase + p0);
-                    dst[0] = make_float4(out[0], out[1], out[2], out[3]);
-                    dst[1] = make_float4(out[4], out[5], out[6], out[7]);
-                }
-            }
-        }
-    };
-
     const uint32_t sbase = tc::smem_u32(sm);
     const uint8_t* ws = reinterpret_cast<const uint8_t*>(a.ws);
     auto tiles_of = [&](int c) { return ws + (((size_t)b * nchunks + c) * s.G + g) * 3 * kTileBytes; };
-    bool ok = true;
-    // the operand tiles are the prologue kernel's output
-    pdl_wait();
-    if (nchunks > 0 && tid == 0) {
-        const uint8_t* src = tiles_of(0);
-        tc::mbar_arrive_expect_tx(bar_a, 2 * kTileBytes);
-        tc::bulk_g2s(sm + L::kBh, src, kTileBytes, bar_a);
-        tc::bulk_g2s(sm + L::kC, src + 2 * kTileBytes, kTileBytes, bar_a);
-        tc::mbar_arrive_expect_tx(bar_b, kTileBytes);
-        tc::bulk_g2s(sm + L::kBl, src + kTileBytes, kTileBytes, bar_b);
-    }
-    if (nchunks > 0) {
-        dt_phase(min(Q, T), dt_raw_next);
-        dt_raw_next = 0.f;
-        if (half == 0 && nchunks > 1 && row < min(Q, T - Q))
-            dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + Q + row) * s.H + h);
-    }
 
-    // The chunk loop is skewed so that CUDA-core work overlaps the tensor cores:
-    // the y epilogue of chunk c-1 runs under chunk c's phase-1 MMAs, and the dt
-    // phase of chunk c+1 under chunk c's phase-2 MMAs.
-    float eS_prev = 0.f;
-    int L_prev = 0, c0_prev = 0;
-    for (int c = 0; c < nchunks; ++c) {
-        const int c0 = c * Q;
-        const int Lc = min(Q, T - c0);
-        const int ksteps = (Lc + 15) / 16;
-        const uint32_t par = c & 1;
-        const bool has_next = c + 1 < nchunks;
-        const int Ln = has_next ? min(Q, T - c0 - Q) : 0;
-        const int Lnn = c + 2 < nchunks ? min(Q, T - c0 - 2 * Q) : 0;
-
-        // 1. this chunk's staged x rows (and its dt phase, done one step earlier)
-        if (!tc::mbar_wait(bar_x, par)) {
-            atomicOr(a.err, ERR_MBAR_TIMEOUT_LOAD);
-            *sFlag = 1;
-        }
-        __syncthreads();
-        if (c == 0 && a.init_conv) {
-            // frames -3..-1 (zero-filled by the copy) come from the initial conv tail
-            constexpr int V = L::kRowBytes / 16;
-            for (int e = tid; e < 3 * V; e += kSsdThreads) {
-                const int r = e / V, q = e % V;
-                *reinterpret_cast<uint4*>(sRaw + (size_t)r * L::kRowBytes + q * 16) =
-                    *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.init_conv) +
-                                                    (((size_t)b * 3 + r) * s.CH() + (size_t)h * P) * sizeof(TA) + q * 16);
-            }
-            __syncthreads();
-        }
-        if (*sFlag) { ok = false; break; }
-        const float Slast = sS[Lc - 1];
-        const float Si = sS[row];
-        const float wi = row < Lc ? __expf(Slast - Si) * sDt[row] : 0.f;
-
-        // 2. conv + SiLU of this head's x channels for row i (staged rows i..i+3)
-        float xf[PH];
-#pragma unroll
-        for (int q8 = 0; q8 < NQ; ++q8) {
-            const int p0 = half * PH + q8 * 8;
-            float o[8];
-            if (row < Lc) {
-                Act8<TA> v[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) v[k].load_rw(sRaw + (size_t)(row + k) * L::kRowBytes, p0);
-                const float4 b0 = reinterpret_cast<const float4*>(sCb + p0)[0];
-                const float4 b1 = reinterpret_cast<const float4*>(sCb + p0)[1];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 w = reinterpret_cast<const float4*>(sCw)[p0 + j];
-                    float acc = j < 4 ? (&b0.x)[j] : (&b1.x)[j - 4];
-                    acc = fmaf(w.x, v[0].get(j), acc);
-                    acc = fmaf(w.y, v[1].get(j), acc);
-                    acc = fmaf(w.z, v[2].get(j), acc);
-                    acc = fmaf(w.w, v[3].get(j), acc);
-                    o[j] = silu_fast(acc);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = 0.f;
-            }
-            uint32_t xh[4], wh[4], wl[4];
-#pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-                xf[q8 * 8 + j] = o[j];
-                xf[q8 * 8 + j + 1] = o[j + 1];
-                xh[j / 2] = pack2(o[j], o[j + 1]);
-                const float w0 = wi * o[j], w1 = wi * o[j + 1];
-                const uint32_t hw = pack2(w0, w1);
-                wh[j / 2] = hw;
-                wl[j / 2] = pack2(w0 - __uint_as_float(hw << 16), w1 - __uint_as_float(hw & 0xFFFF0000u));
-            }
-            const uint32_t off = tc::mn_inter_off(p0, row, P);
-            *reinterpret_cast<uint4*>(sm + L::kX + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
-            *reinterpret_cast<uint4*>(sm + L::kWh + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-            *reinterpret_cast<uint4*>(sm + L::kWl + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        }
-
-        // 3. state: h_prev (bf16) into shared memory for Y_off, then h <- exp(S_last) h in TMEM
-        {
-            const float decay = __expf(Slast);
-            const int n = row;
-            float v[NQ][8];
-#pragma unroll
-            for (int q8 = 0; q8 < NQ; ++q8) tc::tmem_ld8(tm + lane_base + kColState + half * PH + q8 * 8, v[q8]);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int q8 = 0; q8 < NQ; ++q8) {
-                const int p0 = half * PH + q8 * 8;
-                *reinterpret_cast<uint4*>(sm + L::kH + tc::mn_inter_off(p0, n, P)) =
-                    make_uint4(pack2(v[q8][0], v[q8][1]), pack2(v[q8][2], v[q8][3]), pack2(v[q8][4], v[q8][5]),
-                               pack2(v[q8][6], v[q8][7]));
-#pragma unroll
-                for (int q = 0; q < 8; ++q) v[q8][q] *= decay;
-                tc::tmem_st8(tm + lane_base + kColState + p0, v[q8]);
-            }
-            tc::tmem_wait_st();
-        }
-        tc::fence_proxy_async_smem();
-        tc::tc_fence_before();
-        __syncthreads();
-
-        // 4. the staged x rows are consumed: stage the next chunk's while the tensor cores run
-        if (has_next && tid == 32) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, c0 + Q);
-
-        // 5. tensor-core phase 1: G = C~ B~^T (commit), the state terms that read
-        //    B~ lo (commit), then the rest of state += B~^T (w o x~)
-        if (tid == 0) {
-            tc::tc_fence_after();
-            if (!tc::mbar_wait(bar_a, par) || !tc::mbar_wait(bar_b, par)) {
-                atomicOr(a.err, ERR_MBAR_TIMEOUT_LOAD);
-                *sFlag = 1;
-            } else {
-                const uint32_t sC = sbase + L::kC, sBh = sbase + L::kBh, sBl = sbase + L::kBl;
-                const uint32_t sWh = sbase + L::kWh, sWl = sbase + L::kWl;
-                const uint32_t idG = tc::idesc_bf16(128, 128, 0, 0);
-                const uint32_t idS = tc::idesc_bf16(128, P, 1, 1);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
-                    tc::mma_bf16(tm + kColG, tc::sdesc(sC + koff, 0, 1024, 2), tc::sdesc(sBh + koff, 0, 1024, 2), idG,
-                                 ks > 0);
-                }
-                tc::mma_commit(bar_g);
-                for (int ks = 0; ks < ksteps; ++ks)
-                    tc::mma_bf16(tm + kColState, tc::sdesc(sBl + ks * 2048, kPanel, 1024, 2),
-                                 tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
-                tc::mma_commit(bar_bl);
-                for (int ks = 0; ks < ksteps; ++ks) {
-                    const uint64_t dBh = tc::sdesc(sBh + ks * 2048, kPanel, 1024, 2);
-                    tc::mma_bf16(tm + kColState, dBh, tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
-                    tc::mma_bf16(tm + kColState, dBh, tc::sdesc(sWl + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
-                }
-            }
-        }
-
-        // 6. meanwhile: the previous chunk's y (phase 1 touches only the G and
-        //    state columns), then this chunk's D x~ preloaded into the Y_diag
-        //    accumulator that phase 2 adds M x~ onto
-        if (c > 0) y_epilogue(c0_prev, L_prev, eS_prev);
-        {
-            float dx[8];
-#pragma unroll
-            for (int q8 = 0; q8 < NQ; ++q8) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) dx[q] = Dh * xf[q8 * 8 + q];
-                tc::tmem_st8(tm + lane_base + kColYd + half * PH + q8 * 8, dx);
-            }
-            tc::tmem_wait_st();
-        }
-        __syncthreads();
-        if (*sFlag) { ok = false; break; }
-        if (!tc::mbar_wait(bar_g, par) || !tc::mbar_wait(bar_bl, par)) {
-            atomicOr(a.err, ERR_MBAR_TIMEOUT_MMA);
-            *sFlag = 1;
-        }
-        if (__syncthreads_or(*sFlag)) { ok = false; break; }
-        tc::tc_fence_after();
-
-        // 7. M = G o exp(S_i - S_j) dt_j (j <= i) -> bf16, K-major SW128 over the B~ lo tile
-        //    (its readers are done; the remaining state MMAs run meanwhile)
-        {
-            const int i = row;
-            // rows past the chunk end: -inf makes every entry 0
-            const float si2 = i < Lc ? Si * kLog2e : __int_as_float(0xff800000);
-            float gv[4][16];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tc::tmem_ld16(tm + lane_base + kColG + half * 64 + q * 16, gv[q]);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j0 = half * 64 + q * 16;
-                uint32_t pk[8];
-#pragma unroll
-                for (int e4 = 0; e4 < 16; e4 += 4) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(sTj + j0 + e4);
-                    float m[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = j0 + e4 + e;
-                        const float v = gv[q][e4 + e] * ex2_approx(si2 - (&t4.x)[e]);
-                        m[e] = j <= i ? v : 0.f;
-                    }
-                    pk[e4 / 2] = pack2(m[0], m[1]);
-                    pk[e4 / 2 + 1] = pack2(m[2], m[3]);
-                }
-                *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0, kTR)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0 + 8, kTR)) =
-                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            }
-        }
-        tc::fence_proxy_async_smem();
-        tc::tc_fence_before();
-        __syncthreads();
-
-        // 8. tensor-core phase 2: Y_diag += M x~ (onto D x~) and Y_off = C~ h_prev^T
-        if (tid == 0) {
-            tc::tc_fence_after();
-            const uint32_t sM = sbase + L::kBl, sX = sbase + L::kX, sC = sbase + L::kC, sH = sbase + L::kH;
-            const uint32_t idY = tc::idesc_bf16(128, P, 0, 1);
-            for (int ks = 0; ks < ksteps; ++ks) {
-                const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
-                tc::mma_bf16(tm + kColYd, tc::sdesc(sM + koff, 0, 1024, 2), tc::sdesc(sX + ks * 2 * LBO_I, LBO_I, 128, 0),
-                             idY, 1);
-            }
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
-                tc::mma_bf16(tm + kColYo, tc::sdesc(sC + koff, 0, 1024, 2),
-                             tc::sdesc(sH + ks * 2 * LBO_I, LBO_I, 128, 0), idY, ks > 0);
-            }
-            tc::mma_commit(bar_y);
-        }
-
-        // 9. meanwhile: the next chunk's dt phase (the mask above was the last
-        //    reader of this chunk's S, dt and T_j; S_i is kept in a register)
-        if (has_next) {
-            dt_phase(Ln, dt_raw_next);
-            dt_raw_next = 0.f;
-            if (half == 0 && row < Lnn)
-                dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + c0 + 2 * Q + row) * s.H + h);
-        }
-        if (!tc::mbar_wait(bar_y, par)) {
-            atomicOr(a.err, ERR_MBAR_TIMEOUT_MMA);
-            *sFlag = 1;
-        }
-        if (__syncthreads_or(*sFlag)) { ok = false; break; }
-        tc::tc_fence_after();
-        // every operand tile of this chunk is consumed: fetch the next chunk's
-        if (has_next && tid == 0) {
-            const uint8_t* src = tiles_of(c + 1);
+    if (!compute) {
+        // ================================================================ control
+        if (tid == kCtrl && nchunks > 0) {
+            stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, 0);  // x was written before the prologue kernel
+            pdl_wait();                                      // the operand tiles are its output
+            const uint8_t* src = tiles_of(0);
             tc::mbar_arrive_expect_tx(bar_a, 2 * kTileBytes);
             tc::bulk_g2s(sm + L::kBh, src, kTileBytes, bar_a);
             tc::bulk_g2s(sm + L::kC, src + 2 * kTileBytes, kTileBytes, bar_a);
             tc::mbar_arrive_expect_tx(bar_b, kTileBytes);
             tc::bulk_g2s(sm + L::kBl, src + kTileBytes, kTileBytes, bar_b);
+            const uint32_t sC = sbase + L::kC, sBh = sbase + L::kBh, sBl = sbase + L::kBl;
+            const uint32_t sX = sbase + L::kX, sWh = sbase + L::kWh, sWl = sbase + L::kWl, sH = sbase + L::kH;
+            const uint32_t idG = tc::idesc_bf16(128, 128, 0, 0);
+            const uint32_t idS = tc::idesc_bf16(128, P, 1, 1);
+            const uint32_t idY = tc::idesc_bf16(128, P, 0, 1);
+            for (int c = 0; c < nchunks; ++c) {
+                const int c0 = c * Q;
+                const int ksteps = (min(Q, T - c0) + 15) / 16;
+                const uint32_t par = c & 1;
+                const bool has_next = c + 1 < nchunks;
+                const bool ok1 = wait_ok(bar_op1, par, ERR_MBAR_TIMEOUT_MMA);
+                tc::tc_fence_after();
+                // the staged rows are consumed: stage the next chunk's
+                if (has_next && ok1) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, c0 + Q);
+                const bool okt = wait_ok(bar_a, par, ERR_MBAR_TIMEOUT_LOAD) && wait_ok(bar_b, par, ERR_MBAR_TIMEOUT_LOAD);
+                if (ok1 && okt) {
+                    // phase 1: G = C~ B~^T (commit), the state terms that read B~ lo
+                    // (commit), then the rest of state += B~^T (w o x~)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
+                        tc::mma_bf16(tm + kColG, tc::sdesc(sC + koff, 0, 1024, 2), tc::sdesc(sBh + koff, 0, 1024, 2),
+                                     idG, ks > 0);
+                    }
+                    tc::mma_commit(bar_g);
+                    for (int ks = 0; ks < ksteps; ++ks)
+                        tc::mma_bf16(tm + kColState, tc::sdesc(sBl + ks * 2048, kPanel, 1024, 2),
+                                     tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
+                    tc::mma_commit(bar_bl);
+                    for (int ks = 0; ks < ksteps; ++ks) {
+                        const uint64_t dBh = tc::sdesc(sBh + ks * 2048, kPanel, 1024, 2);
+                        tc::mma_bf16(tm + kColState, dBh, tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
+                        tc::mma_bf16(tm + kColState, dBh, tc::sdesc(sWl + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
+                    }
+                }
+                if (wait_ok(bar_op2, par, ERR_MBAR_TIMEOUT_MMA)) {
+                    tc::tc_fence_after();
+                    // phase 2: Y_diag += M x~ (onto D x~) and Y_off = C~ h_prev^T
+                    for (int ks = 0; ks < ksteps; ++ks) {
+                        const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
+                        tc::mma_bf16(tm + kColYd, tc::sdesc(sBl + koff, 0, 1024, 2),
+                                     tc::sdesc(sX + ks * 2 * LBO_I, LBO_I, 128, 0), idY, 1);
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
+                        tc::mma_bf16(tm + kColYo, tc::sdesc(sC + koff, 0, 1024, 2),
+                                     tc::sdesc(sH + ks * 2 * LBO_I, LBO_I, 128, 0), idY, ks > 0);
+                    }
+                    tc::mma_commit(bar_y);
+                }
+                // every operand tile of this chunk is consumed: fetch the next chunk's
+                if (wait_ok(bar_y, par, ERR_MBAR_TIMEOUT_MMA) && has_next) {
+                    const uint8_t* nsrc = tiles_of(c + 1);
+                    tc::mbar_arrive_expect_tx(bar_a, 2 * kTileBytes);
+                    tc::bulk_g2s(sm + L::kBh, nsrc, kTileBytes, bar_a);
+                    tc::bulk_g2s(sm + L::kC, nsrc + 2 * kTileBytes, kTileBytes, bar_a);
+                    tc::mbar_arrive_expect_tx(bar_b, kTileBytes);
+                    tc::bulk_g2s(sm + L::kBl, nsrc + kTileBytes, kTileBytes, bar_b);
+                }
+            }
+            if (*sFlag) {
+                // a wait gave up: let copies still in flight land before the CTA exits
+                for (int i = 0; i < 3; ++i) {
+                    tc::mbar_wait(bar_a + i, 0, 100000000ull);
+                    tc::mbar_wait(bar_a + i, 1, 100000000ull);
+                }
+            }
         }
-        eS_prev = __expf(Si);
-        L_prev = Lc;
-        c0_prev = c0;
+    } else {
+        // ================================================================ compute
+        // initial state -> TMEM [n lanes][p columns]; rows n >= N stay zero
+        {
+            const int n = row;
+#pragma unroll
+            for (int q8 = 0; q8 < NQ; ++q8) {
+                const int p0 = half * PH + q8 * 8;
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    v[q] = (a.init_ssm && n < s.N)
+                               ? __ldg(a.init_ssm + (((size_t)b * s.H + h) * P + p0 + q) * s.N + n)
+                               : 0.f;
+                tc::tmem_st8(tm + lane_base + kColState + p0, v);
+            }
+            tc::tmem_wait_st();
+        }
+        // dt_raw of this thread's row, loaded one chunk ahead of the dt phase that uses it
+        float dt_raw_next = 0.f;
+        if (nchunks > 0 && half == 0 && row < min(Q, T))
+            dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + row) * s.H + h);
+
+        // dt = softplus(dt_raw + dt_bias), a = dt A, inclusive cumulative sum S over
+        // a chunk of Lx rows, and the decay-mask column term in the log2 domain,
+        // T_j = S_j log2e - log2(dt_j) (+inf past the chunk end: dt_j = 0), all
+        // into shared memory. Every compute thread must call it (it holds a barrier).
+        auto dt_phase = [&](int Lx, float raw) {
+            float v = 0.f, dt = 0.f;
+            if (half == 0) {
+                dt = row < Lx ? softplus_f32(raw + dtb) : 0.f;
+                v = dt * A;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, v, off);
+                    if (lane >= off) v += o;
+                }
+                if (lane == 31) sWsum[warp] = v;
+            }
+            compute_sync();
+            if (half == 0) {
+                float add = 0.f;
+                for (int w = 0; w < (row >> 5); ++w) add += sWsum[w];
+                const float S = v + add;
+                sS[row] = S;
+                sDt[row] = dt;
+                sTj[row] = row < Lx ? fmaf(S, kLog2e, -__log2f(dt)) : __int_as_float(0x7f800000);
+            }
+        };
+
+        // y = (D x~ + M x~) + exp(S_i) Y_off for the chunk whose results sit in TMEM.
+        // The TMEM loads are warp-collective (.sync.aligned): every lane issues
+        // them; only the stores are predicated.
+        auto y_epilogue = [&](int c0y, int Ly, float eSy) {
+            const bool live = row < Ly;
+            const size_t ybase = (((size_t)b * T + c0y + row) * s.H + h) * P;
+            float yd[NQ][8], yo[NQ][8];
+#pragma unroll
+            for (int q8 = 0; q8 < NQ; ++q8) {
+                tc::tmem_ld8(tm + lane_base + kColYd + half * PH + q8 * 8, yd[q8]);
+                tc::tmem_ld8(tm + lane_base + kColYo + half * PH + q8 * 8, yo[q8]);
+            }
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int q8 = 0; q8 < NQ; ++q8) {
+                const int p0 = half * PH + q8 * 8;
+                float out[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) out[q] = fmaf(eSy, yo[q8][q], yd[q8][q]);
+                if (live) {
+                    if constexpr (sizeof(TA) == 2) {
+                        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.y) + ybase + p0) =
+                            make_uint4(pack2(out[0], out[1]), pack2(out[2], out[3]), pack2(out[4], out[5]),
+                                       pack2(out[6], out[7]));
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + ybase + p0);
+                        dst[0] = make_float4(out[0], out[1], out[2], out[3]);
+                        dst[1] = make_float4(out[4], out[5], out[6], out[7]);
+                    }
+                }
+            }
+        };
+
+        if (nchunks > 0) {
+            dt_phase(min(Q, T), dt_raw_next);
+            dt_raw_next = 0.f;
+            if (half == 0 && nchunks > 1 && row < min(Q, T - Q))
+                dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + Q + row) * s.H + h);
+        }
+
+        // The chunk loop is skewed so that CUDA-core work overlaps the tensor
+        // cores: the y epilogue of chunk c-1 and the D x~ preload run under
+        // chunk c's phase-1 MMAs, the dt phase of chunk c+1 under its phase 2.
+        float eS_prev = 0.f;
+        int L_prev = 0, c0_prev = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            const int c0 = c * Q;
+            const int Lc = min(Q, T - c0);
+            const uint32_t par = c & 1;
+            const bool has_next = c + 1 < nchunks;
+            const int Ln = has_next ? min(Q, T - c0 - Q) : 0;
+            const int Lnn = c + 2 < nchunks ? min(Q, T - c0 - 2 * Q) : 0;
+
+            // 1. this chunk's staged x rows (its dt phase ran one step earlier)
+            wait_ok(bar_x, par, ERR_MBAR_TIMEOUT_LOAD);
+            compute_sync();
+            if (c == 0 && a.init_conv) {
+                // frames -3..-1 (zero-filled by the copy) come from the initial conv tail
+                constexpr int V = L::kRowBytes / 16;
+                for (int e = tid; e < 3 * V; e += kComputeThreads) {
+                    const int r = e / V, q = e % V;
+                    *reinterpret_cast<uint4*>(sRaw + (size_t)r * L::kRowBytes + q * 16) =
+                        *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.init_conv) +
+                                                        (((size_t)b * 3 + r) * s.CH() + (size_t)h * P) * sizeof(TA) +
+                                                        q * 16);
+                }
+                compute_sync();
+            }
+            const float Slast = sS[Lc - 1];
+            const float Si = sS[row];
+            const float wi = row < Lc ? __expf(Slast - Si) * sDt[row] : 0.f;
+
+            // 2. conv + SiLU of this head's x channels for row i (staged rows i..i+3)
+            float xf[PH];
+#pragma unroll
+            for (int q8 = 0; q8 < NQ; ++q8) {
+                const int p0 = half * PH + q8 * 8;
+                float o[8];
+                if (row < Lc) {
+                    Act8<TA> v[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) v[k].load_rw(sRaw + (size_t)(row + k) * L::kRowBytes, p0);
+                    const float4 b0 = reinterpret_cast<const float4*>(sCb + p0)[0];
+                    const float4 b1 = reinterpret_cast<const float4*>(sCb + p0)[1];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 w = reinterpret_cast<const float4*>(sCw)[p0 + j];
+                        float acc = j < 4 ? (&b0.x)[j] : (&b1.x)[j - 4];
+                        acc = fmaf(w.x, v[0].get(j), acc);
+                        acc = fmaf(w.y, v[1].get(j), acc);
+                        acc = fmaf(w.z, v[2].get(j), acc);
+                        acc = fmaf(w.w, v[3].get(j), acc);
+                        o[j] = silu_fast(acc);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) o[j] = 0.f;
+                }
+                uint32_t xh[4], wh[4], wl[4];
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
+                    xf[q8 * 8 + j] = o[j];
+                    xf[q8 * 8 + j + 1] = o[j + 1];
+                    xh[j / 2] = pack2(o[j], o[j + 1]);
+                    const float w0 = wi * o[j], w1 = wi * o[j + 1];
+                    const uint32_t hw = pack2(w0, w1);
+                    wh[j / 2] = hw;
+                    wl[j / 2] = pack2(w0 - __uint_as_float(hw << 16), w1 - __uint_as_float(hw & 0xFFFF0000u));
+                }
+                const uint32_t off = tc::mn_inter_off(p0, row, P);
+                *reinterpret_cast<uint4*>(sm + L::kX + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+                *reinterpret_cast<uint4*>(sm + L::kWh + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                *reinterpret_cast<uint4*>(sm + L::kWl + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            }
+
+            // 3. state: h_prev (bf16) into shared memory for Y_off, then h <- exp(S_last) h in TMEM
+            {
+                const float decay = __expf(Slast);
+                const int n = row;
+                float v[NQ][8];
+#pragma unroll
+                for (int q8 = 0; q8 < NQ; ++q8) tc::tmem_ld8(tm + lane_base + kColState + half * PH + q8 * 8, v[q8]);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int q8 = 0; q8 < NQ; ++q8) {
+                    const int p0 = half * PH + q8 * 8;
+                    *reinterpret_cast<uint4*>(sm + L::kH + tc::mn_inter_off(p0, n, P)) =
+                        make_uint4(pack2(v[q8][0], v[q8][1]), pack2(v[q8][2], v[q8][3]), pack2(v[q8][4], v[q8][5]),
+                                   pack2(v[q8][6], v[q8][7]));
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q8][q] *= decay;
+                    tc::tmem_st8(tm + lane_base + kColState + p0, v[q8]);
+                }
+                tc::tmem_wait_st();
+            }
+            // hand the phase-1 operands (x~, w o x~ tiles, h tile, scaled state) to the control warp
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::mbar_arrive(bar_op1);
+
+            // 4. meanwhile: the previous chunk's y (phase 1 writes only the G and
+            //    state columns), then this chunk's D x~ preloaded into the Y_diag
+            //    accumulator that phase 2 adds M x~ onto
+            if (c > 0) y_epilogue(c0_prev, L_prev, eS_prev);
+            {
+                float dx[8];
+#pragma unroll
+                for (int q8 = 0; q8 < NQ; ++q8) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) dx[q] = Dh * xf[q8 * 8 + q];
+                    tc::tmem_st8(tm + lane_base + kColYd + half * PH + q8 * 8, dx);
+                }
+                tc::tmem_wait_st();
+            }
+            wait_ok(bar_g, par, ERR_MBAR_TIMEOUT_MMA);
+            wait_ok(bar_bl, par, ERR_MBAR_TIMEOUT_MMA);
+            tc::tc_fence_after();
+
+            // 5. M = G o exp(S_i - S_j) dt_j (j <= i) -> bf16, K-major SW128 over the B~ lo
+            //    tile (its readers are done; the remaining state MMAs run meanwhile)
+            {
+                const int i = row;
+                // rows past the chunk end: -inf makes every entry 0
+                const float si2 = i < Lc ? Si * kLog2e : __int_as_float(0xff800000);
+                float gv[4][16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tc::tmem_ld16(tm + lane_base + kColG + half * 64 + q * 16, gv[q]);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j0 = half * 64 + q * 16;
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int e4 = 0; e4 < 16; e4 += 4) {
+                        const float4 t4 = *reinterpret_cast<const float4*>(sTj + j0 + e4);
+                        float m[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = j0 + e4 + e;
+                            const float v = gv[q][e4 + e] * ex2_approx(si2 - (&t4.x)[e]);
+                            m[e] = j <= i ? v : 0.f;
+                        }
+                        pk[e4 / 2] = pack2(m[0], m[1]);
+                        pk[e4 / 2 + 1] = pack2(m[2], m[3]);
+                    }
+                    *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0, kTR)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0 + 8, kTR)) =
+                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+            }
+            // hand the phase-2 operands (M tile, D x~ in Y_diag) to the control warp
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::mbar_arrive(bar_op2);
+
+            // 6. meanwhile: the next chunk's dt phase (the mask above was the last
+            //    reader of this chunk's S, dt and T_j; S_i is kept in a register)
+            if (has_next) {
+                dt_phase(Ln, dt_raw_next);
+                dt_raw_next = 0.f;
+                if (half == 0 && row < Lnn)
+                    dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + c0 + 2 * Q + row) * s.H + h);
+            }
+            wait_ok(bar_y, par, ERR_MBAR_TIMEOUT_MMA);
+            tc::tc_fence_after();
+            eS_prev = __expf(Si);
+            L_prev = Lc;
+            c0_prev = c0;
+        }
+        // the last chunk's y
+        compute_sync();
+        if (!*sFlag && nchunks > 0) y_epilogue(c0_prev, L_prev, eS_prev);
     }
-    // the last chunk's y
-    if (ok && nchunks > 0) y_epilogue(c0_prev, L_prev, eS_prev);
 
     pdl_trigger();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const bool ok = !*sFlag;
     // final state: TMEM [n][p] -> final_ssm [b,h,p,n]
-    if (ok) {
+    if (ok && compute) {
         const int n = row;
         float v[NQ][8];
 #pragma unroll
@@ -634,12 +662,6 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     a.final_ssm[(((size_t)b * s.H + h) * P + half * PH + q8 * 8 + q) * s.N + n] = v[q8][q];
-        }
-    } else if (tid == 0) {
-        // a wait gave up: let bulk copies still in flight land before the CTA exits
-        for (int i = 0; i < 3; ++i) {
-            tc::mbar_wait(bar_a + i, 0, 100000000ull);
-            tc::mbar_wait(bar_a + i, 1, 100000000ull);
         }
     }
     // final conv tail (the last K-1 pre-conv frames). This CTA owns the tail of
@@ -662,7 +684,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tm, kTmemCols);
+    if (!compute) tc::tmem_dealloc(tm, kTmemCols);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -700,8 +722,13 @@ cudaError_t make_x_map(const ScanArgs& a, CUtensorMap* map) {
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// after_prologue: the launch directly follows this call's prologue kernel on
+// the stream. Only then may the SSD kernel start early (programmatic
+// dependent launch): its reads before griddepcontrol.wait (x, dt_raw, the
+// initial state, the weights) are of data written before the prologue began.
+// Otherwise it is an ordinary launch.
 template <typename TA, int P>
-cudaError_t launch_ssd(const ScanArgs& a, int nchunks, cudaStream_t st) {
+cudaError_t launch_ssd(const ScanArgs& a, int nchunks, bool after_prologue, cudaStream_t st) {
     CUtensorMap tmx;
     memset(&tmx, 0, sizeof(tmx));
     if (nchunks > 0) {
@@ -719,7 +746,10 @@ cudaError_t launch_ssd(const ScanArgs& a, int nchunks, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    return launch_pdl(scan_ssd_kernel<TA, P>, dim3(a.s.H, a.batch), dim3(kSsdThreads), smem, st, a, nchunks, tmx);
+    if (after_prologue && nchunks > 0)
+        return launch_pdl(scan_ssd_kernel<TA, P>, dim3(a.s.H, a.batch), dim3(kSsdThreads), smem, st, a, nchunks, tmx);
+    scan_ssd_kernel<TA, P><<<dim3(a.s.H, a.batch), kSsdThreads, smem, st>>>(a, nchunks, tmx);
+    return cudaGetLastError();
 }
 
 template <typename TA>
@@ -730,14 +760,14 @@ cudaError_t launch_bc_typed(const ScanArgs& a, cudaStream_t st) {
 }
 
 template <typename TA>
-cudaError_t launch_chunks_typed(const ScanArgs& a, cudaStream_t st) {
+cudaError_t launch_chunks_typed(const ScanArgs& a, bool after_prologue, cudaStream_t st) {
     const int nchunks = (a.T + a.chunk - 1) / a.chunk;
     switch (a.s.P) {
-        case 16: return launch_ssd<TA, 16>(a, nchunks, st);
-        case 32: return launch_ssd<TA, 32>(a, nchunks, st);
-        case 48: return launch_ssd<TA, 48>(a, nchunks, st);
-        case 64: return launch_ssd<TA, 64>(a, nchunks, st);
-        case 80: return launch_ssd<TA, 80>(a, nchunks, st);
+        case 16: return launch_ssd<TA, 16>(a, nchunks, after_prologue, st);
+        case 32: return launch_ssd<TA, 32>(a, nchunks, after_prologue, st);
+        case 48: return launch_ssd<TA, 48>(a, nchunks, after_prologue, st);
+        case 64: return launch_ssd<TA, 64>(a, nchunks, after_prologue, st);
+        case 80: return launch_ssd<TA, 80>(a, nchunks, after_prologue, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -755,9 +785,10 @@ cudaError_t launch_scan_prepare(const ScanArgs& a, cudaStream_t st) {
     return a.s.bf16 ? launch_bc_typed<bf16_t>(a, st) : launch_bc_typed<float>(a, st);
 }
 
-cudaError_t launch_scan_chunks(const ScanArgs& a, cudaStream_t st) {
+cudaError_t launch_scan_chunks(const ScanArgs& a, bool after_prologue, cudaStream_t st) {
     if (a.batch == 0) return cudaSuccess;
-    return a.s.bf16 ? launch_chunks_typed<bf16_t>(a, st) : launch_chunks_typed<float>(a, st);
+    return a.s.bf16 ? launch_chunks_typed<bf16_t>(a, after_prologue, st)
+                    : launch_chunks_typed<float>(a, after_prologue, st);
 }
 
 }  // namespace m2
