@@ -451,6 +451,7 @@ def run_gpu(args, world, rank, local):
                   "achieved_gbs": N_LAYERS * STEP_BYTES_PER_SESSION / (frame_us * 1e-6) / 1e9}
     step_frame["frac_hbm"] = step_frame["achieved_gbs"] / peaks["hbm"]
     s64 = _sessions_step_args(m2, torch, dev, layers[0], 64)
+    torch.cuda.synchronize()  # its tensors were made on torch's stream, not `stream`
     torch.cuda.nvtx.range_push("step64")
     s64_us = _time_step_graph(m2, torch, stream, [s64], reps=50)
     torch.cuda.nvtx.range_pop()

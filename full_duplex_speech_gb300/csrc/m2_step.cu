@@ -2,7 +2,7 @@
 // of the persistent "Mamba2 state" that the VoiceChat online session keeps;
 // "docs/nemotron-voicechat.md", section Online session).
 //
-// Two kernels per call, both bound by HBM bandwidth:
+// Two kernels per call, both bound by memory latency or bandwidth:
 //  1. step_conv_kernel: for every (session, channel) the 4-tap causal conv of
 //     the cached tail plus this frame, bias, SiLU -> fp32 scratch; the tail is
 //     shifted in place. Each channel is owned by exactly one thread, so the
@@ -22,6 +22,46 @@
 namespace m2 {
 
 namespace {
+
+// u = SiLU(conv_b + sum_k w[k] * window[k]) for 8 consecutive channels from
+// c; the window is the cached tail (t-3, t-2, t-1) and this frame. All weight
+// loads are issued before any arithmetic, so they overlap one another.
+template <typename TA>
+__device__ __forceinline__ void conv_silu8(const StepArgs& a, long c, const Act8<TA> (&tail)[3],
+                                           const Act8<TA>& cur, float (&out)[8]) {
+    const float4* w4 = reinterpret_cast<const float4*>(a.conv_w + c * 4);
+    float4 w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = __ldg(w4 + j);
+    const float4 b0 = __ldg(reinterpret_cast<const float4*>(a.conv_b + c));
+    const float4 b1 = __ldg(reinterpret_cast<const float4*>(a.conv_b + c) + 1);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float u = j < 4 ? (&b0.x)[j] : (&b1.x)[j - 4];
+        u = fmaf(w[j].x, tail[0].get(j), u);
+        u = fmaf(w[j].y, tail[1].get(j), u);
+        u = fmaf(w[j].z, tail[2].get(j), u);
+        u = fmaf(w[j].w, cur.get(j), u);
+        out[j] = silu_fast(u);
+    }
+}
+
+// The tail after this frame: the oldest frame drops out, this frame enters.
+template <typename TA>
+__device__ __forceinline__ void shift_tail(const StepArgs& a, int ses, long c, const Act8<TA> (&tail)[3],
+                                           const Act8<TA>& cur) {
+    const long CH = a.s.CH();
+    tail[1].store(a.conv, ((size_t)ses * 3 + 0) * CH + c);
+    tail[2].store(a.conv, ((size_t)ses * 3 + 1) * CH + c);
+    cur.store(a.conv, ((size_t)ses * 3 + 2) * CH + c);
+}
+
+template <typename TA>
+__device__ __forceinline__ void load_tail(const StepArgs& a, int ses, long c, Act8<TA> (&tail)[3]) {
+    const long CH = a.s.CH();
+#pragma unroll
+    for (int k = 0; k < 3; ++k) tail[k].load_rw(a.conv, ((size_t)ses * 3 + k) * CH + c);
+}
 
 constexpr int kConvThreads = 64;
 
@@ -44,31 +84,14 @@ __global__ void __launch_bounds__(kConvThreads) step_conv_kernel(StepArgs a) {
             cur.load(a.B, (size_t)ses * GN + (c - HP));
         else
             cur.load(a.C, (size_t)ses * GN + (c - HP - GN));
-        // cached tail: frames t-3, t-2, t-1
         Act8<TA> tail[3];
-#pragma unroll
-        for (int k = 0; k < 3; ++k) tail[k].load_rw(a.conv, ((size_t)ses * 3 + k) * CH + c);
-        const float4* w4 = reinterpret_cast<const float4*>(a.conv_w + c * 4);
-        const float4 b0 = __ldg(reinterpret_cast<const float4*>(a.conv_b + c));
-        const float4 b1 = __ldg(reinterpret_cast<const float4*>(a.conv_b + c) + 1);
+        load_tail<TA>(a, ses, c, tail);
         float out[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float4 w = __ldg(w4 + j);
-            float u = j < 4 ? (&b0.x)[j] : (&b1.x)[j - 4];
-            u = fmaf(w.x, tail[0].get(j), u);
-            u = fmaf(w.y, tail[1].get(j), u);
-            u = fmaf(w.z, tail[2].get(j), u);
-            u = fmaf(w.w, cur.get(j), u);
-            out[j] = silu_f32(u);
-        }
+        conv_silu8<TA>(a, c, tail, cur, out);
         float4* dst = reinterpret_cast<float4*>(a.ws_u + (size_t)ses * CH + c);
         dst[0] = make_float4(out[0], out[1], out[2], out[3]);
         dst[1] = make_float4(out[4], out[5], out[6], out[7]);
-        // shift the tail: oldest frame drops out, this frame enters
-        tail[1].store(a.conv, ((size_t)ses * 3 + 0) * CH + c);
-        tail[2].store(a.conv, ((size_t)ses * 3 + 1) * CH + c);
-        cur.store(a.conv, ((size_t)ses * 3 + 2) * CH + c);
+        shift_tail<TA>(a, ses, c, tail, cur);
     } else if (v - nvec < s.H) {
         const int h = (int)(v - nvec);
         const float z = load_act<TA>(a.dt_raw, (size_t)ses * s.H + h) + __ldg(a.dt_bias + h);

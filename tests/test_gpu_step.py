@@ -34,7 +34,7 @@ def _frame(inp, t):
 def _gpu_step(m2, d, S, frame, pdev, ssm_dev, conv_dev, act):
     import torch
     dims = m2.dims(0, 0, d.H, d.P, d.N, d.G, d.K, act)
-    ws = torch.empty(m2.mamba2_step_workspace_bytes(dims, S), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(m2.mamba2_step_workspace_bytes(dims, S), dtype=torch.uint8, device="cuda")
     y = act_empty((S, d.H, d.P), act)
     fd = {k: to_dev(frame[k]) for k in ("x", "B", "C", "dt_raw")}
     m2.mamba2_step(dims, S, fd["x"], fd["B"], fd["C"], fd["dt_raw"], pdev["A_log"], pdev["D"],
@@ -135,3 +135,23 @@ def test_step_rejects_bad_arguments_on_gpu(m2):
                           check=False) == 3
     # workspace too small
     assert m2.mamba2_step(dims, 1, *args, ws, workspace_bytes=16, check=False) == 6
+
+
+@pytest.mark.parametrize("S", [1, 8, 15, 16])
+def test_step_session_counts_real_shape(m2, S):
+    """1 to 16 sessions at the real shape, each from its own random state,
+    against the oracle, conv tail included."""
+    import oracle
+    d, act = REAL_SHAPE, "bf16"
+    inp = mixer_inputs(110 + S, d, S, 1, act)
+    ssm0 = ssm_state_inputs(111, d, S, scale=0.2)
+    conv0 = conv_state_inputs(112, d, S, act)
+    ssm_dev, conv_dev = to_dev(ssm0), to_dev(conv0)
+    y = _gpu_step(m2, d, S, _frame(inp, 0), _params_dev(inp), ssm_dev, conv_dev, act)
+    ssm_ref = ssm0.astype(np.float64).copy()
+    conv_ref = as_f64(conv0, act).copy()
+    y_ref = oracle.mixer_step(d, _frame(inp, 0), inp, ssm_ref, conv_ref, nthreads=0)
+    assert y_error(from_dev_act(y, act), y_ref, act) <= Y_TOL
+    assert state_error(ssm_dev.cpu().numpy(), ssm_ref) <= STATE_TOL
+    exp_tail = _tail_bits(conv0, _frame(inp, 0), d)
+    np.testing.assert_array_equal(bits_of(conv_dev), np.ascontiguousarray(exp_tail).view(np.uint8).reshape(-1))
