@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nch
 
     float out[kBcRows][8];
     if (real && r0 < L) {
-        // pre-conv rows r0-3 .. r0+3, all loads issued before any use
+        // pre-conv rows r0-3 .. r0+3, weights and bias: all loads issued before any use
         float win[kBcRows + 3][8];
 #pragma unroll
         for (int k = 0; k < kBcRows + 3; ++k) {
@@ -85,10 +85,15 @@ __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nch
 #pragma unroll
             for (int j = 0; j < 8; ++j) win[k][j] = have ? v.get(j) : 0.f;
         }
+        float4 w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = __ldg(reinterpret_cast<const float4*>(a.conv_w) + ch0 + j);
+        const float4 b0 = __ldg(reinterpret_cast<const float4*>(a.conv_b + ch0));
+        const float4 b1 = __ldg(reinterpret_cast<const float4*>(a.conv_b + ch0) + 1);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float4 wj = __ldg(reinterpret_cast<const float4*>(a.conv_w) + ch0 + j);
-            const float bj = __ldg(a.conv_b + ch0 + j);
+            const float4 wj = w[j];
+            const float bj = j < 4 ? (&b0.x)[j] : (&b1.x)[j - 4];
 #pragma unroll
             for (int r = 0; r < kBcRows; ++r) {
                 float u = bj;
