@@ -56,6 +56,8 @@ def load():
         for f in ("mamba2_conv_scan", "mamba2_scan_prepare_bc", "mamba2_scan_chunks"):
             getattr(lib, f).argtypes = [dp] + [vp] * 9 + [ip] + [vp] * 6 + [sz, vp]
             getattr(lib, f).restype = ip
+        lib.mamba2_conv_scan_varlen.argtypes = [dp] + [vp] * 10 + [ip] + [vp] * 6 + [sz, vp]
+        lib.mamba2_conv_scan_varlen.restype = ip
         lib.mamba2_step_workspace_bytes.argtypes = [dp, ip]
         lib.mamba2_step_workspace_bytes.restype = sz
         lib.mamba2_step.argtypes = [dp, ip] + [vp] * 13 + [sz, vp]
@@ -140,6 +142,21 @@ def mamba2_conv_scan(d: M2Dims, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv
                      stream=None, check=True) -> int:
     return _scan_call("mamba2_conv_scan", d, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk,
                       init_ssm, init_conv, y, final_ssm, final_conv, workspace, workspace_bytes, stream, check)
+
+
+def mamba2_conv_scan_varlen(d: M2Dims, lengths, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk,
+                            init_ssm, init_conv, y, final_ssm, final_conv, workspace, workspace_bytes=None,
+                            stream=None, check=True) -> int:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
+    rc = load().mamba2_conv_scan_varlen(
+        ctypes.byref(d), _p(lengths), _p(x), _p(B), _p(C), _p(dt_raw), _p(A_log), _p(D), _p(dt_bias),
+        _p(conv_w), _p(conv_b), int(chunk), _p(init_ssm), _p(init_conv), _p(y), _p(final_ssm), _p(final_conv),
+        _p(workspace), int(workspace_bytes), _stream(stream))
+    if check and rc:
+        raise M2Error(rc, "mamba2_conv_scan_varlen")
+    return rc
 
 
 def mamba2_scan_prepare_bc(d: M2Dims, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk,

@@ -215,6 +215,7 @@ m2_status scan_setup(const m2_dims* d, const void* x, const void* B, const void*
     a->ws = workspace;
     a->ws_bytes = workspace_bytes;
     a->err = g_dev_error_ptr[dev];
+    a->lens = nullptr;
     return M2_OK;
 }
 
@@ -244,6 +245,24 @@ m2_status mamba2_scan_chunks(M2_SCAN_PARAMS) {
     m2_status st = scan_setup(M2_SCAN_ARGS, &a);
     if (st != M2_OK || d->batch == 0) return st;
     cudaError_t e = m2::launch_scan_chunks(a, false, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M2_OK : cuda_fail(e);
+}
+
+m2_status mamba2_conv_scan_varlen(const m2_dims* d, const int* lengths, const void* x, const void* B,
+                                  const void* C, const void* dt_raw, const float* A_log, const float* D,
+                                  const float* dt_bias, const float* conv_w, const float* conv_b, int chunk,
+                                  const float* init_ssm, const void* init_conv, void* y, float* final_ssm,
+                                  void* final_conv, void* workspace, size_t workspace_bytes, void* stream) {
+    if (d && d->batch > 0) {
+        if (!lengths) return M2_EINVAL;
+        if ((reinterpret_cast<uintptr_t>(lengths) & 3u) != 0) return M2_EALIGN;
+    }
+    m2::ScanArgs a;
+    m2_status st = scan_setup(M2_SCAN_ARGS, &a);
+    if (st != M2_OK || d->batch == 0) return st;
+    a.lens = lengths;
+    cudaError_t e = m2::launch_scan_prepare(a, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = m2::launch_scan_chunks(a, true, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M2_OK : cuda_fail(e);
 }
 

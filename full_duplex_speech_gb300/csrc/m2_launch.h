@@ -44,6 +44,7 @@ struct ScanArgs {
     void* ws;
     size_t ws_bytes;
     unsigned int* err;  // device error word
+    const int* lens;    // [batch] frames used per sequence, device (NULL: T for all)
 };
 
 // Records a CUDA error for mamba2_last_cuda_error() on the calling thread.

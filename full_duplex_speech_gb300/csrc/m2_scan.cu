@@ -40,6 +40,12 @@ constexpr int kNP = 128;                       // state dimension padded to the 
 constexpr uint32_t kTileBytes = kTR * kNP * 2;  // one bf16 operand tile, 32 KiB
 constexpr uint32_t kPanel = kTR * 128;          // one 64-column panel of a tile, 16 KiB
 
+// Frames used by sequence b: its entry of the lengths array clamped to
+// [0, T], or T. Strides always use T.
+__device__ __forceinline__ int seq_len(const ScanArgs& a, int b) {
+    return a.lens ? min(max(__ldg(a.lens + b), 0), a.T) : a.T;
+}
+
 // ----------------------------------------------------------------- kernel 1
 constexpr int kBcThreads = 256;
 constexpr int kBcRows = 4;  // rows per thread; a CTA covers 32 rows of one (chunk, group)
@@ -50,7 +56,6 @@ __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nch
     const int c = blockIdx.x >> 2, quarter = blockIdx.x & 3, g = blockIdx.y, b = blockIdx.z;
     const int T = a.T, Q = a.chunk;
     const int c0 = c * Q;
-    const int L = min(Q, T - c0);
     const long HP = s.HP(), GN = s.GN(), CH = s.CH();
     uint8_t* tiles = reinterpret_cast<uint8_t*>(a.ws) + (((size_t)b * nchunks + c) * s.G + g) * 3 * kTileBytes;
     uint8_t* tBh = tiles;
@@ -65,7 +70,9 @@ __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nch
     const bool real = n0 < s.N;
     const long ch0 = HP + which * GN + (long)g * s.N + n0;  // conv channel of n0
     const void* src = which ? a.C : a.B;
-    pdl_wait();  // B and C may come from the previous kernel
+    pdl_wait();  // B, C and the lengths may come from the previous kernel
+    const int L = min(Q, seq_len(a, b) - c0);  // rows of this chunk in the sequence
+    if (L <= 0) return;                        // past the sequence end: no tile is read
 
     float out[kBcRows][8];
     if (real && r0 < L) {
@@ -130,19 +137,20 @@ __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nch
     pdl_trigger();  // at the end, so waiting SSD CTAs do not crowd this grid off the SMs
 }
 
-// The final conv tail of 8 channels [c, c+8) of sequence b: frames T-3..T-1,
-// taken from the initial tail (or zeros) where T < 3. Every source slot is
-// read before any is written, so final_conv may alias init_conv.
+// The final conv tail of 8 channels [c, c+8) of sequence b: frames Tb-3..Tb-1
+// (Tb = its length), taken from the initial tail (or zeros) where Tb < 3.
+// Every source slot is read before any is written, so final_conv may alias
+// init_conv.
 template <typename TA>
 __device__ void write_tail(const ScanArgs& a, int b, long c) {
     const Shape& s = a.s;
     const long CH = s.CH(), HP = s.HP(), GN = s.GN();
-    const int T = a.T;
+    const int T = a.T, Tb = seq_len(a, b);
     Act8<TA> vals[3];
     bool zero[3];
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
-        const int t = T - 3 + k;
+        const int t = Tb - 3 + k;
         zero[k] = false;
         if (t >= 0) {
             if (c < HP)
@@ -244,6 +252,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     const int h = blockIdx.x, b = blockIdx.y;
     const int g = h / (s.H / s.G);
     const int T = a.T, Q = a.chunk;
+    // this sequence's frames and chunks (the workspace is laid out for nchunks)
+    const int Tb = seq_len(a, b);
+    const int nchb = (Tb + Q - 1) / Q;
     const long HP = s.HP();
     const int tid = threadIdx.x, row = tid & 127, half = (tid >> 7) & 1, warp = tid >> 5, lane = tid & 31;
     const bool compute = tid < kComputeThreads;
@@ -306,7 +317,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
 
     if (!compute) {
         // ================================================================ control
-        if (tid == kCtrl && nchunks > 0) {
+        if (tid == kCtrl && nchb > 0) {
             stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, 0);  // x was written before the prologue kernel
             pdl_wait();                                      // the operand tiles are its output
             const uint8_t* src = tiles_of(0);
@@ -320,11 +331,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             const uint32_t idG = tc::idesc_bf16(128, 128, 0, 0);
             const uint32_t idS = tc::idesc_bf16(128, P, 1, 1);
             const uint32_t idY = tc::idesc_bf16(128, P, 0, 1);
-            for (int c = 0; c < nchunks; ++c) {
+            for (int c = 0; c < nchb; ++c) {
                 const int c0 = c * Q;
-                const int ksteps = (min(Q, T - c0) + 15) / 16;
+                const int ksteps = (min(Q, Tb - c0) + 15) / 16;
                 const uint32_t par = c & 1;
-                const bool has_next = c + 1 < nchunks;
+                const bool has_next = c + 1 < nchb;
                 const bool ok1 = wait_ok(bar_op1, par, ERR_MBAR_TIMEOUT_MMA);
                 tc::tc_fence_after();
                 // the staged rows are consumed: stage the next chunk's
@@ -404,7 +415,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         }
         // dt_raw of this thread's row, loaded one chunk ahead of the dt phase that uses it
         float dt_raw_next = 0.f;
-        if (nchunks > 0 && half == 0 && row < min(Q, T))
+        if (nchb > 0 && half == 0 && row < min(Q, Tb))
             dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + row) * s.H + h);
 
         // dt = softplus(dt_raw + dt_bias), a = dt A, inclusive cumulative sum S over
@@ -467,10 +478,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             }
         };
 
-        if (nchunks > 0) {
-            dt_phase(min(Q, T), dt_raw_next);
+        if (nchb > 0) {
+            dt_phase(min(Q, Tb), dt_raw_next);
             dt_raw_next = 0.f;
-            if (half == 0 && nchunks > 1 && row < min(Q, T - Q))
+            if (half == 0 && nchb > 1 && row < min(Q, Tb - Q))
                 dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + Q + row) * s.H + h);
         }
 
@@ -479,13 +490,13 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         // chunk c's phase-1 MMAs, the dt phase of chunk c+1 under its phase 2.
         float eS_prev = 0.f;
         int L_prev = 0, c0_prev = 0;
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = 0; c < nchb; ++c) {
             const int c0 = c * Q;
-            const int Lc = min(Q, T - c0);
+            const int Lc = min(Q, Tb - c0);
             const uint32_t par = c & 1;
-            const bool has_next = c + 1 < nchunks;
-            const int Ln = has_next ? min(Q, T - c0 - Q) : 0;
-            const int Lnn = c + 2 < nchunks ? min(Q, T - c0 - 2 * Q) : 0;
+            const bool has_next = c + 1 < nchb;
+            const int Ln = has_next ? min(Q, Tb - c0 - Q) : 0;
+            const int Lnn = c + 2 < nchb ? min(Q, Tb - c0 - 2 * Q) : 0;
 
             // 1. this chunk's staged x rows (its dt phase ran one step earlier)
             wait_ok(bar_x, par, ERR_MBAR_TIMEOUT_LOAD);
@@ -646,7 +657,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         }
         // the last chunk's y
         compute_sync();
-        if (!*sFlag && nchunks > 0) y_epilogue(c0_prev, L_prev, eS_prev);
+        if (!*sFlag && nchb > 0) y_epilogue(c0_prev, L_prev, eS_prev);
     }
 
     pdl_trigger();

@@ -108,6 +108,27 @@ m2_status mamba2_conv_scan(const m2_dims* d, const void* x, const void* B, const
                            float* final_ssm, void* final_conv, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* mamba2_conv_scan over a batch of sequences of different lengths: catching
+ * up several sessions at once, or prefilling prompts of different lengths
+ * (each optionally continuing from its own cached state), padded to one T.
+ *
+ * lengths: device int32 [d->batch], 4-byte aligned; sequence b uses frames
+ *   [0, lengths[b]) of its T-frame slots of x, B, C, dt_raw. Values are read
+ *   on the device (so they may be produced by earlier work on the stream) and
+ *   clamped to [0, T].
+ * y: rows t < lengths[b] of sequence b are written; rows at or past it are
+ *   left as they were.
+ * final_ssm / final_conv: the states after frame lengths[b] - 1 (for a
+ *   length of 0, the initial states, copied).
+ * Everything else (arguments, layouts, workspace, aliasing, tolerances,
+ * errors) is that of mamba2_conv_scan; a NULL lengths returns M2_EINVAL.
+ * With every length equal to T the results are those of mamba2_conv_scan. */
+m2_status mamba2_conv_scan_varlen(const m2_dims* d, const int* lengths, const void* x, const void* B,
+                                  const void* C, const void* dt_raw, const float* A_log, const float* D,
+                                  const float* dt_bias, const float* conv_w, const float* conv_b, int chunk,
+                                  const float* init_ssm, const void* init_conv, void* y, float* final_ssm,
+                                  void* final_conv, void* workspace, size_t workspace_bytes, void* stream);
+
 /* The two halves of mamba2_conv_scan, with the same arguments, for callers
  * that schedule or time them separately. mamba2_conv_scan(args) is exactly
  * mamba2_scan_prepare_bc(args) followed by mamba2_scan_chunks(args) on the

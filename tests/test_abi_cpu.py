@@ -86,6 +86,19 @@ def test_scan_validation_without_gpu(m2):
     assert m2.mamba2_conv_scan(neg, *p, 16, None, None, *outs, **ok) == 1
 
 
+def test_varlen_scan_validation_without_gpu(m2):
+    d = m2.dims(2, 64, 4, 16, 16, 1, 4, "f32")
+    p = _fake_ptrs(9)
+    outs = _fake_ptrs(3, base=1 << 24)
+    ok = dict(workspace=1 << 30, workspace_bytes=1 << 40, stream=0, check=False)
+    lens = 1 << 28
+    assert m2.mamba2_conv_scan_varlen(d, None, *p, 16, None, None, *outs, **ok) == 1      # no lengths
+    assert m2.mamba2_conv_scan_varlen(d, lens + 2, *p, 16, None, None, *outs, **ok) == 3  # misaligned
+    assert m2.mamba2_conv_scan_varlen(d, lens, *p, 0, None, None, *outs, **ok) == 1       # chunk < 1
+    bad = m2.dims(2, 64, 4, 16, 16, 1, 5, "f32")
+    assert m2.mamba2_conv_scan_varlen(bad, lens, *p, 16, None, None, *outs, **ok) == 2
+
+
 def test_workspace_queries(m2):
     d = m2.dims(4, 4096, 128, 80, 128, 8, 4, "bf16")
     assert m2.mamba2_step_workspace_bytes(d, 64) >= 64 * (12288 + 128) * 4

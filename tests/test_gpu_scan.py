@@ -161,3 +161,97 @@ def test_long_prefill_sampled_heads(m2):
     d = REAL_SHAPE
     inp = mixer_inputs(400, d, 4, 4096, "bf16")
     check(m2, d, inp, 128, 4, 4096, heads=(77, 79))
+
+
+# ------------------------------------------------------ variable-length batches
+SENTINEL = 0x5A5A  # bit pattern left in y rows a call must not write
+
+
+def gpu_scan_varlen(m2, d, inp, chunk, lengths, init_ssm=None, init_conv=None):
+    """Runs mamba2_conv_scan_varlen; returns (y, final_ssm, final_conv) device tensors."""
+    import torch
+    act = inp["act"]
+    batch, T = inp["x"].shape[:2]
+    dims = m2.dims(batch, T, d.H, d.P, d.N, d.G, d.K, act)
+    dev = {k: to_dev(inp[k]) for k in ("x", "B", "C", "dt_raw", "A_log", "D", "dt_bias", "conv_w", "conv_b")}
+    lens = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    y = act_empty((batch, T, d.H, d.P), act)
+    y.view(torch.int16 if act == "bf16" else torch.int32).fill_(SENTINEL)
+    fs = torch.empty((batch, d.H, d.P, d.N), dtype=torch.float32, device="cuda")
+    fc = act_empty((batch, d.K - 1, d.CH), act)
+    ws = torch.empty(max(m2.mamba2_scan_workspace_bytes(dims, chunk), 16), dtype=torch.uint8, device="cuda")
+    m2.mamba2_conv_scan_varlen(dims, lens, dev["x"], dev["B"], dev["C"], dev["dt_raw"], dev["A_log"], dev["D"],
+                               dev["dt_bias"], dev["conv_w"], dev["conv_b"], chunk,
+                               None if init_ssm is None else to_dev(init_ssm),
+                               None if init_conv is None else to_dev(init_conv), y, fs, fc, ws)
+    torch.cuda.synchronize()
+    assert m2.mamba2_device_error() == 0
+    return y, fs, fc
+
+
+def check_varlen(m2, d, inp, chunk, lengths, init_ssm=None, init_conv=None):
+    """Every sequence against the oracle run on its own frames only."""
+    import oracle
+    act = inp["act"]
+    y, fs, fc = gpu_scan_varlen(m2, d, inp, chunk, lengths, init_ssm, init_conv)
+    y_bits = bits_of(y).view(np.uint16 if act == "bf16" else np.uint32).reshape(y.shape)
+    y_all = from_dev_act(y, act)
+    fs_all, fc_bits = fs.cpu().numpy(), bits_of(fc).reshape(len(lengths), -1)
+    for b, L in enumerate(lengths):
+        sub = dict(inp, **{k: np.ascontiguousarray(inp[k][b:b + 1, :L]) for k in ("x", "B", "C", "dt_raw")})
+        iss = None if init_ssm is None else init_ssm[b:b + 1]
+        ic = None if init_conv is None else init_conv[b:b + 1]
+        ref = oracle.mixer_scan(d, sub, init_ssm=iss, init_conv=ic)
+        if L > 0:
+            assert y_error(y_all[b:b + 1, :L], ref["y"], act) <= Y_TOL, b
+        assert np.all(y_bits[b, L:] == SENTINEL), b  # rows past the length are left alone
+        if L == 0:  # the initial state passes through unchanged
+            want = np.zeros_like(fs_all[b]) if iss is None else iss[0]
+            np.testing.assert_array_equal(fs_all[b], want)
+        else:
+            assert state_error(fs_all[b:b + 1], ref["final_ssm"]) <= STATE_TOL, b
+        np.testing.assert_array_equal(fc_bits[b], expected_tail_bits(sub, d, ic).view(np.uint8).reshape(-1))
+
+
+@pytest.mark.parametrize("chunk", [16, 32])
+def test_varlen_ragged_batch(m2, chunk):
+    d = Dims(H=8, P=32, N=64, G=2)
+    lengths = [100, 0, 1, 2, chunk - 1, chunk, chunk + 1, 77]
+    inp = mixer_inputs(70 + chunk, d, len(lengths), 100, "bf16")
+    check_varlen(m2, d, inp, chunk, lengths)
+
+
+def test_varlen_continuing_sessions(m2):
+    """Sessions catching up from their own cached states, different lengths."""
+    d = Dims(H=8, P=80, N=128, G=2)
+    lengths = [45, 0, 3, 16, 17, 2]
+    inp = mixer_inputs(80, d, len(lengths), 45, "bf16")
+    iss, ic = _prefix_state(d, 81, len(lengths), 60, "bf16")
+    check_varlen(m2, d, inp, 16, lengths, init_ssm=iss, init_conv=ic)
+
+
+def test_varlen_real_shape(m2):
+    d = REAL_SHAPE
+    lengths = [300, 128, 129, 7]
+    inp = mixer_inputs(90, d, len(lengths), 300, "bf16")
+    check_varlen(m2, d, inp, 128, lengths)
+
+
+def test_varlen_full_lengths_equal_the_plain_scan(m2):
+    """All lengths = T: bit-identical to mamba2_conv_scan."""
+    d = Dims(H=8, P=32, N=64, G=2)
+    inp = mixer_inputs(95, d, 3, 70, "bf16")
+    y0, fs0, fc0 = gpu_scan(m2, d, inp, 32, 3, 70)
+    y1, fs1, fc1 = gpu_scan_varlen(m2, d, inp, 32, [70, 70, 70])
+    for a_, b_ in ((y0, y1), (fs0, fs1), (fc0, fc1)):
+        np.testing.assert_array_equal(bits_of(a_), bits_of(b_))
+
+
+def test_varlen_lengths_are_clamped(m2):
+    """Lengths below 0 act as 0, above T as T."""
+    d = Dims(H=4, P=16, N=16, G=1)
+    inp = mixer_inputs(96, d, 2, 40, "f32")
+    y, fs, fc = gpu_scan_varlen(m2, d, inp, 16, [-5, 1000])
+    y1, fs1, fc1 = gpu_scan_varlen(m2, d, inp, 16, [0, 40])
+    for a_, b_ in ((y, y1), (fs, fs1), (fc, fc1)):
+        np.testing.assert_array_equal(bits_of(a_), bits_of(b_))
