@@ -336,14 +336,12 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 const int ksteps = (min(Q, Tb - c0) + 15) / 16;
                 const uint32_t par = c & 1;
                 const bool has_next = c + 1 < nchb;
-                const bool ok1 = wait_ok(bar_op1, par, ERR_MBAR_TIMEOUT_MMA);
-                tc::tc_fence_after();
-                // the staged rows are consumed: stage the next chunk's
-                if (has_next && ok1) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, c0 + Q);
-                const bool okt = wait_ok(bar_a, par, ERR_MBAR_TIMEOUT_LOAD) && wait_ok(bar_b, par, ERR_MBAR_TIMEOUT_LOAD);
-                if (ok1 && okt) {
-                    // phase 1: G = C~ B~^T (commit), the state terms that read B~ lo
-                    // (commit), then the rest of state += B~^T (w o x~)
+                // G = C~ B~^T as soon as the tiles are in: it needs nothing from the
+                // compute warps, and its TMEM columns were last read by the previous
+                // chunk's mask (before that chunk's phase-2 handoff)
+                const bool okt = wait_ok(bar_a, par, ERR_MBAR_TIMEOUT_LOAD);
+                if (okt) {
+                    tc::tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
@@ -351,6 +349,15 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                                      idG, ks > 0);
                     }
                     tc::mma_commit(bar_g);
+                }
+                const bool ok1 = wait_ok(bar_op1, par, ERR_MBAR_TIMEOUT_MMA);
+                tc::tc_fence_after();
+                // the staged rows are consumed: stage the next chunk's
+                if (has_next && ok1) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, c0 + Q);
+                const bool okb = wait_ok(bar_b, par, ERR_MBAR_TIMEOUT_LOAD);
+                if (ok1 && okt && okb) {
+                    // phase 1: the state terms that read B~ lo (commit), then the
+                    // rest of state += B~^T (w o x~)
                     for (int ks = 0; ks < ksteps; ++ks)
                         tc::mma_bf16(tm + kColState, tc::sdesc(sBl + ks * 2048, kPanel, 1024, 2),
                                      tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
