@@ -195,8 +195,13 @@ struct SsdSmem {
     static constexpr uint32_t kWh = kX + kPT;             // (w o x~) hi
     static constexpr uint32_t kWl = kWh + kPT;            // (w o x~) lo
     static constexpr uint32_t kH = kWl + kPT;             // h hi            (MN-major interleave, K = n)
-    static constexpr uint32_t kRaw = kH + kPT;            // pre-conv x rows [kRawRows][P] (act dtype)
-    static constexpr uint32_t kRowBytes = P * sizeof(TA);
+    static constexpr uint32_t kRaw = kH + kPT;            // pre-conv x rows [kRawRows][P + pad] (act dtype)
+    // bf16 rows carry 8 channels of padding (the next head's, or zeros past the
+    // last): an odd number of 16-byte units per row, so the 32 rows a warp reads
+    // at once fall on distinct bank groups
+    static constexpr int kRawPad = sizeof(TA) == 2 ? 8 : 0;
+    static constexpr uint32_t kRowBytes = (P + kRawPad) * sizeof(TA);
+    static constexpr uint32_t kRowData = P * sizeof(TA);  // the head's own channels
     static constexpr uint32_t kS = kRaw + kRawRows * kRowBytes;  // float S[128]
     static constexpr uint32_t kDt = kS + 512;             // float dt[128]
     static constexpr uint32_t kTj = kDt + 512;            // float S_j log2e - log2(dt_j) [128]
@@ -510,7 +515,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             compute_sync();
             if (c == 0 && a.init_conv) {
                 // frames -3..-1 (zero-filled by the copy) come from the initial conv tail
-                constexpr int V = L::kRowBytes / 16;
+                constexpr int V = L::kRowData / 16;
                 for (int e = tid; e < 3 * V; e += kComputeThreads) {
                     const int r = e / V, q = e % V;
                     *reinterpret_cast<uint4*>(sRaw + (size_t)r * L::kRowBytes + q * 16) =
@@ -729,7 +734,8 @@ EncodeTiledFn encode_tiled() {
 }
 
 // x viewed as a 3-D tensor [b][T][H*P] (innermost last); a box is the
-// [kRawRows x P] pre-conv rows of one head for one chunk.
+// [kRawRows x (P + pad)] pre-conv rows of one head for one chunk (the pad
+// channels belong to the next head, or lie past the end and read as zero).
 template <typename TA, int P>
 cudaError_t make_x_map(const ScanArgs& a, CUtensorMap* map) {
     EncodeTiledFn enc = encode_tiled();
@@ -737,7 +743,7 @@ cudaError_t make_x_map(const ScanArgs& a, CUtensorMap* map) {
     const cuuint64_t HP = (cuuint64_t)a.s.H * P;
     const cuuint64_t dims[3] = {HP, (cuuint64_t)a.T, (cuuint64_t)a.batch};
     const cuuint64_t strides[2] = {HP * sizeof(TA), HP * (cuuint64_t)a.T * sizeof(TA)};
-    const cuuint32_t box[3] = {(cuuint32_t)P, (cuuint32_t)kRawRows, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)(P + SsdSmem<TA, P>::kRawPad), (cuuint32_t)kRawRows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapDataType dt = sizeof(TA) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     CUresult r = enc(map, dt, 3, const_cast<void*>(a.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
