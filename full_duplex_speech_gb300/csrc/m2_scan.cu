@@ -204,7 +204,7 @@ struct SsdSmem {
     static constexpr uint32_t kRowData = P * sizeof(TA);  // the head's own channels
     static constexpr uint32_t kS = kRaw + kRawRows * kRowBytes;  // float S[128]
     static constexpr uint32_t kDt = kS + 512;             // float dt[128]
-    static constexpr uint32_t kTj = kDt + 512;            // float S_j log2e - log2(dt_j) [128]
+    static constexpr uint32_t kTj = kDt + 512;            // float exp(S_j1 - S_j) dt_j, j1 = j | 7 [128]
     static constexpr uint32_t kWsum = kTj + 512;          // float warp sums[8]
     static constexpr uint32_t kCw = kWsum + 64;           // float conv_w[P][4]
     static constexpr uint32_t kCb = kCw + P * 16;         // float conv_b[P]
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
 
     float* sS = reinterpret_cast<float*>(sm + L::kS);
     float* sDt = reinterpret_cast<float*>(sm + L::kDt);
-    float* sTj = reinterpret_cast<float*>(sm + L::kTj);
+    float* sEb = reinterpret_cast<float*>(sm + L::kTj);
     float* sWsum = reinterpret_cast<float*>(sm + L::kWsum);
     float* sCw = reinterpret_cast<float*>(sm + L::kCw);
     float* sCb = reinterpret_cast<float*>(sm + L::kCb);
@@ -431,9 +431,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + row) * s.H + h);
 
         // dt = softplus(dt_raw + dt_bias), a = dt A, inclusive cumulative sum S over
-        // a chunk of Lx rows, and the decay-mask column term in the log2 domain,
-        // T_j = S_j log2e - log2(dt_j) (+inf past the chunk end: dt_j = 0), all
-        // into shared memory. Every compute thread must call it (it holds a barrier).
+        // a chunk of Lx rows, and the column factor of the decay mask,
+        // Eb_j = exp(S_j1 - S_j) dt_j with j1 = j | 7 the last column of j's
+        // 8-column block (0 past the chunk end, where dt_j = 0), all into shared
+        // memory. S does not increase, so Eb_j <= dt_j. Every compute thread
+        // must call it (it holds barriers).
         auto dt_phase = [&](int Lx, float raw) {
             float v = 0.f, dt = 0.f;
             if (half == 0) {
@@ -453,8 +455,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 const float S = v + add;
                 sS[row] = S;
                 sDt[row] = dt;
-                sTj[row] = row < Lx ? fmaf(S, kLog2e, -__log2f(dt)) : __int_as_float(0x7f800000);
             }
+            compute_sync();
+            if (half == 0) sEb[row] = ex2_approx((sS[row | 7] - sS[row]) * kLog2e) * sDt[row];
         };
 
         // y = (D x~ + M x~) + exp(S_i) Y_off for the chunk whose results sit in TMEM.
@@ -616,11 +619,23 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             tc::tc_fence_after();
 
             // 5. M = G o exp(S_i - S_j) dt_j (j <= i) -> bf16, K-major SW128 over the B~ lo
-            //    tile (its readers are done; the remaining state MMAs run meanwhile)
+            //    tile (its readers are done; the remaining state MMAs run meanwhile).
+            //    An 8-column block [j0, j1] wholly left of row i factors as
+            //    exp(S_i - S_j1) * Eb_j, both factors <= 1 (S does not increase);
+            //    the block holding the diagonal takes one exponential per entry.
             {
                 const int i = row;
-                // rows past the chunk end: -inf makes every entry 0
-                const float si2 = i < Lc ? Si * kLog2e : __int_as_float(0xff800000);
+                const bool live = i < Lc;
+                const int jd = i & ~7;                 // this row's diagonal block
+                const bool dg_here = (jd >> 6) == half;  // uniform across the warp
+                float dg[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dg[e] = 0.f;
+                if (dg_here && live) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (jd + e <= i) dg[e] = ex2_approx((Si - sS[jd + e]) * kLog2e) * sDt[jd + e];
+                }
                 float gv[4][16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) tc::tmem_ld16(tm + lane_base + kColG + half * 64 + q * 16, gv[q]);
@@ -630,17 +645,22 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                     const int j0 = half * 64 + q * 16;
                     uint32_t pk[8];
 #pragma unroll
-                    for (int e4 = 0; e4 < 16; e4 += 4) {
-                        const float4 t4 = *reinterpret_cast<const float4*>(sTj + j0 + e4);
-                        float m[4];
+                    for (int e8 = 0; e8 < 16; e8 += 8) {
+                        const int jb = j0 + e8;
+                        // row factor of a block left of the diagonal (0 for dead rows)
+                        const float ea = (live && jb < jd) ? ex2_approx((Si - sS[jb + 7]) * kLog2e) : 0.f;
+                        const float4 c0 = *reinterpret_cast<const float4*>(sEb + jb);
+                        const float4 c1 = *reinterpret_cast<const float4*>(sEb + jb + 4);
+                        float m[8];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int j = j0 + e4 + e;
-                            const float v = gv[q][e4 + e] * ex2_approx(si2 - (&t4.x)[e]);
-                            m[e] = j <= i ? v : 0.f;
+                        for (int e = 0; e < 8; ++e) {
+                            const float eb = e < 4 ? (&c0.x)[e] : (&c1.x)[e - 4];
+                            m[e] = gv[q][e8 + e] * (jb == jd ? dg[e] : eb * ea);
                         }
-                        pk[e4 / 2] = pack2(m[0], m[1]);
-                        pk[e4 / 2 + 1] = pack2(m[2], m[3]);
+                        pk[e8 / 2 + 0] = pack2(m[0], m[1]);
+                        pk[e8 / 2 + 1] = pack2(m[2], m[3]);
+                        pk[e8 / 2 + 2] = pack2(m[4], m[5]);
+                        pk[e8 / 2 + 3] = pack2(m[6], m[7]);
                     }
                     *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0, kTR)) =
                         make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -654,7 +674,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             tc::mbar_arrive(bar_op2);
 
             // 6. meanwhile: the next chunk's dt phase (the mask above was the last
-            //    reader of this chunk's S, dt and T_j; S_i is kept in a register)
+            //    reader of this chunk's S, dt and Eb; S_i is kept in a register)
             if (has_next) {
                 dt_phase(Ln, dt_raw_next);
                 dt_raw_next = 0.f;
