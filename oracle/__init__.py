@@ -66,7 +66,9 @@ def _load():
             lib.m2o_conv_tail.argtypes = [ctypes.POINTER(_Dims)] + [dp] * 5
             lib.m2o_mixer_scan.argtypes = [ctypes.POINTER(_Dims)] + [dp] * 14 + [ip] * 4
             lib.m2o_mixer_step.argtypes = [ctypes.POINTER(_Dims), ip] + [dp] * 12 + [ip]
-            for f in ("m2o_ssm", "m2o_conv_silu", "m2o_conv_tail", "m2o_mixer_scan", "m2o_mixer_step"):
+            lib.m2o_gated_norm.argtypes = [ip, ip, ip, dp, dp, dp, ctypes.c_double, dp]
+            for f in ("m2o_ssm", "m2o_conv_silu", "m2o_conv_tail", "m2o_mixer_scan", "m2o_mixer_step",
+                      "m2o_gated_norm"):
                 getattr(lib, f).restype = ip
             _lib = lib
     return _lib
@@ -184,3 +186,16 @@ def mixer_step(d: Dims, frame: dict, params: dict, ssm_state, conv_state, nthrea
         _ptr(conv_state), _ptr(y), nthreads)
     _check(rc, "mixer_step")
     return y
+
+
+def gated_norm(y, z, weight, groups: int, eps: float = 1e-5) -> np.ndarray:
+    """Gated RMSNorm: y, z [..., width] (fp64 values), weight [width]; the
+    last axis is split into `groups` contiguous blocks. Returns fp64."""
+    y, z = _f64(y), _f64(z)
+    width = y.shape[-1]
+    rows = int(np.prod(y.shape[:-1])) if y.ndim > 1 else 1
+    out = np.empty_like(y)
+    rc = _load().m2o_gated_norm(rows, width, int(groups), _ptr(y), _ptr(z), _ptr(_f64(weight)), float(eps),
+                                _ptr(out))
+    _check(rc, "gated_norm")
+    return out

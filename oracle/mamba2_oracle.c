@@ -339,3 +339,34 @@ int m2o_mixer_step(const m2o_dims* d, int S, const double* x, const double* B, c
     }
     return err;
 }
+
+/* Gated RMSNorm of the mixer output (the standard Mamba-2 output norm; the
+ * VoiceChat issue, section config.json / text_config, gives rms_norm_eps
+ * 1e-5). For each of `rows` positions and each of `groups` contiguous blocks
+ * of width/groups channels:
+ *     v   = y * silu(z)
+ *     out = weight * v / sqrt(mean over the block of v^2 + eps)
+ * y, z, out [rows, width]; weight [width]. */
+int m2o_gated_norm(int rows, int width, int groups, const double* y, const double* z,
+                   const double* weight, double eps, double* out) {
+    if (rows < 0 || width <= 0 || groups <= 0 || width % groups != 0 || !y || !z || !weight || !out ||
+        !(eps >= 0.0))
+        return M2O_EINVAL;
+    const int gw = width / groups;
+    double* v = (double*)malloc(sizeof(double) * (size_t)gw);
+    if (!v) return M2O_ENOMEM;
+    for (long r = 0; r < rows; ++r) {
+        for (int g = 0; g < groups; ++g) {
+            const long base = r * width + (long)g * gw;
+            double ss = 0.0;
+            for (int k = 0; k < gw; ++k) {
+                v[k] = y[base + k] * m2o_silu(z[base + k]);
+                ss += v[k] * v[k];
+            }
+            const double inv = 1.0 / sqrt(ss / gw + eps);
+            for (int k = 0; k < gw; ++k) out[base + k] = weight[(long)g * gw + k] * v[k] * inv;
+        }
+    }
+    free(v);
+    return M2O_OK;
+}

@@ -352,3 +352,54 @@ def test_bf16_codec_roundtrip():
     assert bf16_bits_to_f64(b64)[3] == 1.0 + 2 ** -7
     assert abs(bf16_bits_to_f64(b64)[4] - 3.140625) == 0.0
     np.testing.assert_array_equal(b32[[0, 1, 2, 3, 4, 6, 7]], b64[[0, 1, 2, 3, 4, 6, 7]])
+
+
+# ------------------------------------------------------------ gated RMSNorm
+def test_gated_norm_open_gate_is_torch_rms_norm():
+    """With a wide-open gate (z = 1000: silu(z) = z exactly in fp64) the
+    gated norm is the library RMSNorm of each channel group, scaled by the
+    weight; the factor 1000 moves into eps (rms_norm of 1000 v with eps e is
+    rms_norm of v with eps e / 1e6)."""
+    import oracle
+    rng = np.random.default_rng(7)
+    rows, width, groups, eps = 5, 48, 3, 1e-5
+    y = rng.standard_normal((rows, width))
+    w = 1 + 0.1 * rng.standard_normal(width)
+    out = oracle.gated_norm(y, np.full_like(y, 1000.0), w, groups, eps)
+    gw = width // groups
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(y).reshape(rows, groups, gw), (gw,), eps=eps / 1e6)
+    ref = ref.reshape(rows, width).numpy() * w
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def test_gated_norm_worked_case():
+    """y = (3, 4), open gate, one group, eps 0: (3, 4) / sqrt(12.5)."""
+    import oracle
+    out = oracle.gated_norm(np.array([[3.0, 4.0]]), np.array([[1000.0, 1000.0]]), np.ones(2), 1, 0.0)
+    np.testing.assert_allclose(out[0], [3 / np.sqrt(12.5), 4 / np.sqrt(12.5)], rtol=1e-15)
+
+
+def test_gated_norm_gate_and_invariances():
+    """The gate multiplies by silu(z) (library expit), the output does not
+    change when y is scaled (eps 0), flips sign with y, and each channel
+    group is normalised on its own."""
+    import oracle
+    rng = np.random.default_rng(8)
+    rows, width, groups = 4, 40, 5
+    y, z = rng.standard_normal((rows, width)), rng.standard_normal((rows, width))
+    w = 1 + 0.1 * rng.standard_normal(width)
+    out = oracle.gated_norm(y, z, w, groups, 0.0)
+    # gate through the library sigmoid: gated input y * z * expit(z), open gate
+    gated = y * z * expit(z)
+    np.testing.assert_allclose(out, oracle.gated_norm(gated, np.full_like(y, 1000.0), w, groups, 0.0) ,
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.gated_norm(7.5 * y, z, w, groups, 0.0), out, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.gated_norm(-y, z, w, groups, 0.0), -out, rtol=1e-12, atol=1e-12)
+    y2 = y.copy()
+    y2[:, :8] *= 3.0  # the first group only
+    out2 = oracle.gated_norm(y2, z, w, groups, 0.0)
+    np.testing.assert_allclose(out2[:, 8:], out[:, 8:], rtol=1e-12, atol=1e-12)
+    assert np.max(np.abs(out2[:, :8] - out[:, :8])) < 1e-12  # scale-free within the group too
+    # each group has mean square (weight-free) 1
+    unit = oracle.gated_norm(y, z, np.ones(width), groups, 0.0).reshape(rows, groups, -1)
+    np.testing.assert_allclose(np.mean(unit ** 2, axis=-1), 1.0, rtol=1e-12)
