@@ -316,6 +316,26 @@ def _time_step_graph(m2, torch, stream, arg_list, reps):
     return e0.elapsed_time(e1) * 1e3 / reps
 
 
+def _time_graph(torch, stream, fn, reps):
+    """Average microseconds of one fn() (which enqueues on `stream`),
+    captured as one CUDA graph and replayed `reps` times."""
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
 def _sessions_step_args(m2, torch, dev, L, S):
     """mamba2_step arguments for S sessions of layer L's weights, with random
     states (the timing does not depend on their values)."""
@@ -461,6 +481,30 @@ def run_gpu(args, world, rank, local):
     del s64
     torch.cuda.synchronize()
 
+    # the gated output norm over the T=300 rows of a scan's y (8 buffer sets
+    # cycled, 147 MB, larger than L2)
+    d = REAL_SHAPE
+    gn = torch.Generator(device=dev).manual_seed(77)
+    norm_sets = [(torch.randn((T_FRAMES, d.H * d.P), generator=gn, device=dev).to(torch.bfloat16),
+                  torch.randn((T_FRAMES, d.H * d.P), generator=gn, device=dev).to(torch.bfloat16),
+                  1 + 0.1 * torch.randn(d.H * d.P, generator=gn, device=dev),
+                  torch.empty((T_FRAMES, d.H * d.P), dtype=torch.bfloat16, device=dev)) for _ in range(8)]
+    torch.cuda.synchronize()
+
+    def norm_pass():
+        for yv, zv, wv, ov in norm_sets:
+            m2.mamba2_gated_norm(layers[0].dims, T_FRAMES, yv, zv, wv, 1e-5, ov, stream=stream)
+
+    torch.cuda.nvtx.range_push("gated_norm")
+    norm_us = _time_graph(torch, stream, norm_pass, reps=50) / len(norm_sets)
+    torch.cuda.nvtx.range_pop()
+    norm_bytes = T_FRAMES * d.H * d.P * 6 + d.H * d.P * 4
+    gated_norm = {"rows": T_FRAMES, "us_per_call": norm_us, "bytes_per_call": norm_bytes,
+                  "achieved_gbs": norm_bytes / (norm_us * 1e-6) / 1e9}
+    gated_norm["frac_hbm"] = gated_norm["achieved_gbs"] / peaks["hbm"]
+    del norm_sets
+    torch.cuda.synchronize()
+
     # end to end through the C ABI with host buffers (eager, public calls)
     e2e = None
     if rank == 0 or True:
@@ -522,6 +566,7 @@ def run_gpu(args, world, rank, local):
                      "sessions": 1},
             "step_frame_b1": step_frame,
             "step_64_sessions": step64,
+            "gated_norm_T300": gated_norm,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": 4 * K,

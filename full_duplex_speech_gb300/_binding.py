@@ -58,6 +58,8 @@ def load():
             getattr(lib, f).restype = ip
         lib.mamba2_conv_scan_varlen.argtypes = [dp] + [vp] * 10 + [ip] + [vp] * 6 + [sz, vp]
         lib.mamba2_conv_scan_varlen.restype = ip
+        lib.mamba2_gated_norm.argtypes = [dp, ip, vp, vp, vp, ctypes.c_float, vp, vp]
+        lib.mamba2_gated_norm.restype = ip
         lib.mamba2_step_workspace_bytes.argtypes = [dp, ip]
         lib.mamba2_step_workspace_bytes.restype = sz
         lib.mamba2_step.argtypes = [dp, ip] + [vp] * 13 + [sz, vp]
@@ -172,6 +174,14 @@ def mamba2_scan_chunks(d: M2Dims, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, co
                        stream=None, check=True) -> int:
     return _scan_call("mamba2_scan_chunks", d, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, chunk,
                       init_ssm, init_conv, y, final_ssm, final_conv, workspace, workspace_bytes, stream, check)
+
+
+def mamba2_gated_norm(d: M2Dims, rows, y, z, weight, eps, out, stream=None, check=True) -> int:
+    rc = load().mamba2_gated_norm(ctypes.byref(d), int(rows), _p(y), _p(z), _p(weight), float(eps), _p(out),
+                                  _stream(stream))
+    if check and rc:
+        raise M2Error(rc, "mamba2_gated_norm")
+    return rc
 
 
 def mamba2_step(d: M2Dims, n_sessions, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, ssm_state,

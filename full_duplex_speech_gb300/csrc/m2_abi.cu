@@ -2,6 +2,7 @@
 // shape and alignment validation on the host, then dispatch to the kernel
 // launchers. Nothing here allocates device memory.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "../../include/mamba2.h"
@@ -112,6 +113,32 @@ m2_status mamba2_device_error(void* stream, unsigned int* code) {
 size_t mamba2_step_workspace_bytes(const m2_dims* d, int n_sessions) {
     if (check_dims(d, false) != M2_OK || n_sessions < 0) return 0;
     return m2::step_workspace_bytes(shape_of(d), n_sessions);
+}
+
+m2_status mamba2_gated_norm(const m2_dims* d, int rows, const void* y, const void* z, const float* weight,
+                            float eps, void* out, void* stream) {
+    m2_status st = check_dims(d, false);
+    if (st != M2_OK) return st;
+    if (rows < 0 || !(eps >= 0.f) || !(eps < INFINITY)) return M2_EINVAL;
+    if ((long)d->nheads / d->ngroups * d->headdim > 32768) return M2_EUNSUPPORTED;
+    const void* ptrs[] = {y, z, weight, out};
+    for (const void* p : ptrs)
+        if (!p) return M2_EINVAL;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return M2_EALIGN;
+    int dev = 0;
+    st = current_device(&dev);
+    if (st != M2_OK) return st;
+    m2::NormArgs a;
+    a.s = shape_of(d);
+    a.rows = rows;
+    a.y = y;
+    a.z = z;
+    a.weight = weight;
+    a.eps = eps;
+    a.out = out;
+    cudaError_t e = m2::launch_gated_norm(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M2_OK : cuda_fail(e);
 }
 
 m2_status mamba2_step(const m2_dims* d, int n_sessions, const void* x, const void* B,

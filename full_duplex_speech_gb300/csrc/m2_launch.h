@@ -47,6 +47,19 @@ struct ScanArgs {
     const int* lens;    // [batch] frames used per sequence, device (NULL: T for all)
 };
 
+struct NormArgs {
+    Shape s;
+    int rows;  // positions
+    const void* y;
+    const void* z;
+    const float* weight;
+    float eps;
+    void* out;
+};
+
+// Gated RMSNorm of the mixer output (y * silu(z), grouped RMS, weight).
+cudaError_t launch_gated_norm(const NormArgs& a, cudaStream_t st);
+
 // Records a CUDA error for mamba2_last_cuda_error() on the calling thread.
 void record_cuda_error(cudaError_t e);
 

@@ -154,6 +154,27 @@ m2_status mamba2_scan_chunks(const m2_dims* d, const void* x, const void* B, con
                              float* final_ssm, void* final_conv, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/* Gated RMSNorm of the mixer output: the standard Mamba-2 output norm that
+ * follows the mixer core in each Mamba layer (the VoiceChat issue
+ * "feat(nemotron_voicechat): load the VoiceChat checkpoint and run offline
+ * duplex inference", section config.json / text_config, gives
+ * rms_norm_eps 1e-5; the pages do not spell out its form, this is the
+ * standard one). For each of `rows` positions and each of d->ngroups
+ * contiguous blocks of H*P/ngroups channels:
+ *     v   = y * silu(z)
+ *     out = weight * v / sqrt(mean over the block of v^2 + eps)
+ * computed in fp32 and rounded once to the activation dtype.
+ *
+ * y, z, out: [rows, H*P] (act dtype; any batch x time flattening of the
+ *   scan's y [b,T,H,P] or the step's y [S,H,P]); out may alias y or z.
+ * weight: [H*P] fp32. eps >= 0 and finite.
+ * Errors: M2_EINVAL (NULL pointer, rows < 0, bad eps, bad dims), M2_ESHAPE,
+ * M2_EUNSUPPORTED (groups wider than 32768 channels), M2_EALIGN (a pointer
+ * not 16-byte aligned), M2_ECUDA. rows == 0 is a no-op once the arguments
+ * check out. Asynchronous on `stream`. */
+m2_status mamba2_gated_norm(const m2_dims* d, int rows, const void* y, const void* z, const float* weight,
+                            float eps, void* out, void* stream);
+
 /* Bytes of device scratch that mamba2_step needs for n_sessions sessions. */
 size_t mamba2_step_workspace_bytes(const m2_dims* d, int n_sessions);
 

@@ -43,6 +43,7 @@ __all__ = [
     "as_f64",
     "conv_state_inputs",
     "ssm_state_inputs",
+    "norm_inputs",
 ]
 
 
@@ -207,3 +208,15 @@ def device_mixer_inputs(seed: int, d: Dims, batch: int, T: int, device, act: str
     out["conv_b"] = uniform((d.CH,), -0.5, 0.5).float()
     out["act"] = act
     return out
+
+
+def norm_inputs(seed: int, d: Dims, rows: int, act: str = "bf16") -> dict:
+    """Inputs of the gated output norm: y, z [rows, H*P] ~ N(0, 1) (act dtype
+    bit patterns for bf16), weight [H*P] ~ 1 + N(0, 0.1) fp32."""
+    rng = np.random.default_rng([seed, 0x5EED, 5])
+    y = rng.standard_normal((rows, d.H * d.P), dtype=np.float32)
+    z = rng.standard_normal((rows, d.H * d.P), dtype=np.float32)
+    w = (1.0 + 0.1 * rng.standard_normal(d.H * d.P)).astype(np.float32)
+    if act == "bf16":
+        y, z = f32_to_bf16_bits(y), f32_to_bf16_bits(z)
+    return dict(y=y, z=z, weight=w, act=act)

@@ -105,3 +105,17 @@ def test_workspace_queries(m2):
     assert m2.mamba2_step_workspace_bytes(d, -1) == 0
     assert m2.mamba2_scan_workspace_bytes(d, 0) == 0
     assert m2.mamba2_scan_workspace_bytes(m2.dims(1, 8, 4, 16, 16, 1, 3, "f32"), 8) == 0
+
+
+def test_gated_norm_validation_without_gpu(m2):
+    d = m2.dims(0, 0, 4, 16, 16, 2, 4, "bf16")
+    p = _fake_ptrs(4)
+    assert m2.mamba2_gated_norm(d, 3, None, p[1], p[2], 1e-5, p[3], stream=0, check=False) == 1  # NULL y
+    assert m2.mamba2_gated_norm(d, -1, *p[:3], 1e-5, p[3], stream=0, check=False) == 1       # rows < 0
+    assert m2.mamba2_gated_norm(d, 3, *p[:3], -1.0, p[3], stream=0, check=False) == 1        # eps < 0
+    assert m2.mamba2_gated_norm(d, 3, *p[:3], float("inf"), p[3], stream=0, check=False) == 1
+    assert m2.mamba2_gated_norm(d, 3, p[0] + 4, *p[1:3], 1e-5, p[3], stream=0, check=False) == 3  # misaligned
+    bad = m2.dims(0, 0, 6, 16, 16, 4, 4, "bf16")  # H not a multiple of G
+    assert m2.mamba2_gated_norm(bad, 3, *p[:3], 1e-5, p[3], stream=0, check=False) == 2
+    wide = m2.dims(0, 0, 512, 80, 16, 1, 4, "bf16")  # a 40960-channel group
+    assert m2.mamba2_gated_norm(wide, 3, *p[:3], 1e-5, p[3], stream=0, check=False) == 4
