@@ -40,7 +40,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from seeded_inputs import MAMBA_LAYERS, REAL_SHAPE, mixer_inputs  # noqa: E402
+from seeded_inputs import MAMBA_LAYERS, REAL_SHAPE, device_mixer_inputs, mixer_inputs  # noqa: E402
 
 T_FRAMES = 300
 CHUNK = 128
@@ -505,6 +505,45 @@ def run_gpu(args, world, rank, local):
     del norm_sets
     torch.cuda.synchronize()
 
+    # long prefill: one layer at batch 4, T=4096 (the parity tests run all 27
+    # layers of it); the whole scan and its SSD kernel alone, CUDA events
+    PB, PT = 4, 4096
+    pf = device_mixer_inputs(4242, d, PB, PT, dev)
+    pdims = m2.dims(PB, PT, d.H, d.P, d.N, d.G, d.K, "bf16")
+    py = torch.empty((PB, PT, d.H, d.P), dtype=torch.bfloat16, device=dev)
+    pfs = torch.empty((PB, d.H, d.P, d.N), device=dev)
+    pfc = torch.empty((PB, d.K - 1, d.CH), dtype=torch.bfloat16, device=dev)
+    pws = torch.empty(m2.mamba2_scan_workspace_bytes(pdims, CHUNK), dtype=torch.uint8, device=dev)
+    pargs = (pdims, pf["x"], pf["B"], pf["C"], pf["dt_raw"], pf["A_log"], pf["D"], pf["dt_bias"], pf["conv_w"],
+             pf["conv_b"], CHUNK, None, None, py, pfs, pfc, pws)
+    torch.cuda.synchronize()
+    pev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+    torch.cuda.nvtx.range_push("prefill")
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            m2.mamba2_conv_scan(*pargs, stream=stream)
+        pev[0].record(stream)
+        for _ in range(5):
+            m2.mamba2_conv_scan(*pargs, stream=stream)
+        pev[1].record(stream)
+        for k in range(3):
+            m2.mamba2_scan_prepare_bc(*pargs, stream=stream)
+            pev[2 + 2 * k].record(stream)
+            m2.mamba2_scan_chunks(*pargs, stream=stream)
+            pev[3 + 2 * k].record(stream)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    pf_ms = pev[0].elapsed_time(pev[1]) / 5
+    pf_ssd_ms = sum(pev[2 + 2 * k].elapsed_time(pev[3 + 2 * k]) for k in range(3)) / 3
+    pf_bytes = SCAN_BYTES_PER_TOKEN * PB * PT + PB * (STATE_BYTES + TAIL_BYTES)
+    pf_flops = SCAN_FLOPS_PER_TOKEN * PB * PT
+    prefill = {"batch": PB, "T": PT, "chunk": CHUNK, "ms_per_layer": pf_ms, "tokens_per_s": PB * PT / (pf_ms * 1e-3),
+               "ssd_ms": pf_ssd_ms,
+               "ssd_frac_hbm": pf_bytes / (pf_ssd_ms * 1e-3) / 1e9 / peaks["hbm"],
+               "ssd_frac_bf16": pf_flops / (pf_ssd_ms * 1e-3) / 1e12 / peaks["bf16"]}
+    del pf, py, pfs, pfc, pws
+    torch.cuda.synchronize()
+
     # end to end through the C ABI with host buffers (eager, public calls)
     e2e = None
     if rank == 0 or True:
@@ -567,6 +606,7 @@ def run_gpu(args, world, rank, local):
             "step_frame_b1": step_frame,
             "step_64_sessions": step64,
             "gated_norm_T300": gated_norm,
+            "prefill_b4_T4096": prefill,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": 4 * K,
