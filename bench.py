@@ -59,7 +59,7 @@ WORKLOAD = ("Nemotron-H Mamba2 mixer, real shape H=128 P=80 N=128 G=8 K=4, batch
 # launch of this workload, from the ncu capture summarised in
 # profiles/scan_ssd_kernel_b1_T300.md. It describes one version of the kernel
 # source; for any other version the traffic is reported as unknown (null).
-SSD_TRAFFIC = {"bytes": 8889600, "m2_scan_cu_sha1": "f9f2bf5dc0ec4e19453905a9aaf90d59f8069dbb"}
+SSD_TRAFFIC = {"bytes": 8884992, "m2_scan_cu_sha1": "4e06345d66a7d21f94790bfba38854f54201a765"}
 SCAN_BYTES_PER_TOKEN = 45312
 STATE_BYTES = 128 * 80 * 128 * 4
 TAIL_BYTES = 3 * 12288 * 2

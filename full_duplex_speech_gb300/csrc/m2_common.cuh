@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
 #include <utility>
 
 namespace m2 {
@@ -20,12 +21,46 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 }
 
 // 8 consecutive activations -> fp32 (16 B of bf16 or 32 B of fp32).
+// Read-only loads issued exactly where they stand. A volatile asm statement
+// with a memory clobber is not moved by the compiler, so a load placed ahead
+// of a barrier or a long wait is in flight during it instead of being sunk
+// to its first use.
+__device__ __forceinline__ uint4 ldg_pinned_u4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p)
+                 : "memory");
+    return r;
+}
+__device__ __forceinline__ float4 ldg_pinned_f4(const void* p) {
+    float4 r;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p)
+                 : "memory");
+    return r;
+}
+__device__ __forceinline__ float ldg_pinned_f32(const void* p) {
+    float r;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(p) : "memory");
+    return r;
+}
+__device__ __forceinline__ uint16_t ldg_pinned_u16(const void* p) {
+    uint16_t r;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p) : "memory");
+    return r;
+}
+
 template <typename TA> struct Act8;
 
 template <> struct Act8<bf16_t> {
     uint4 raw;
     __device__ __forceinline__ void load(const void* base, size_t elem) {
         raw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(base) + elem));
+    }
+    __device__ __forceinline__ void load_pinned(const void* base, size_t elem) {
+        raw = ldg_pinned_u4(reinterpret_cast<const uint16_t*>(base) + elem);
     }
     // plain (coherent) load, for data that this kernel also writes
     __device__ __forceinline__ void load_rw(const void* base, size_t elem) {
@@ -46,6 +81,11 @@ template <> struct Act8<float> {
         const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + elem);
         a = __ldg(p);
         b = __ldg(p + 1);
+    }
+    __device__ __forceinline__ void load_pinned(const void* base, size_t elem) {
+        const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + elem);
+        a = ldg_pinned_f4(p);
+        b = ldg_pinned_f4(p + 1);
     }
     __device__ __forceinline__ void load_rw(const void* base, size_t elem) {
         const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + elem);
@@ -74,6 +114,22 @@ template <> __device__ __forceinline__ float load_act<bf16_t>(const void* base, 
 }
 template <> __device__ __forceinline__ float load_act<float>(const void* base, size_t elem) {
     return __ldg(reinterpret_cast<const float*>(base) + elem);
+}
+
+// One activation element as stored (bf16 bits or fp32), loaded where it
+// stands and not converted yet, so that nothing waits on it until raw_to_f32.
+template <typename TA> using ActRaw = typename std::conditional<sizeof(TA) == 2, uint16_t, float>::type;
+template <typename TA> __device__ __forceinline__ ActRaw<TA> load_raw_pinned(const void* base, size_t elem) {
+    if constexpr (sizeof(TA) == 2)
+        return ldg_pinned_u16(reinterpret_cast<const uint16_t*>(base) + elem);
+    else
+        return ldg_pinned_f32(reinterpret_cast<const float*>(base) + elem);
+}
+template <typename TA> __device__ __forceinline__ float raw_to_f32(ActRaw<TA> r) {
+    if constexpr (sizeof(TA) == 2)
+        return bf16_bits_to_float(r);
+    else
+        return r;
 }
 
 // softplus(z) = log(1 + e^z), evaluated without overflow on either side.

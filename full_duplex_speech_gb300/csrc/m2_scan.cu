@@ -17,8 +17,8 @@
 //        y       = M x~ + exp(S_i) Y_off + D x~              (tcgen05, bf16)
 //     The conv + SiLU of the head's own x channels, softplus(dt) and the
 //     cumulative sums run on the CUDA cores between the tensor-core phases.
-//     At its end each CTA also writes its share of the final conv tail (the
-//     last K-1 pre-conv frames).
+//     Each CTA also writes its share of the final conv tail (the last K-1
+//     pre-conv frames).
 //
 // The chunked form is the state-space-duality (SSD) evaluation of the Mamba-2
 // recurrence (Dao & Gu 2024): the intra-chunk part is a masked quadratic form,
@@ -47,94 +47,114 @@ __device__ __forceinline__ int seq_len(const ScanArgs& a, int b) {
 }
 
 // ----------------------------------------------------------------- kernel 1
+// This kernel lets the SSD kernel launch as soon as every CTA here has passed its
+// griddepcontrol.wait: SSD CTAs then start at once on SMs without a CTA of
+// this kernel, and on each other SM as soon as its CTA here exits. (An SSD
+// CTA cannot share an SM with these CTAs: three of its nine warps, at 168
+// registers, nearly fill one sub-partition's register file.) Two rows per
+// thread keep each CTA short.
 constexpr int kBcThreads = 256;
-constexpr int kBcRows = 4;  // rows per thread; a CTA covers 32 rows of one (chunk, group)
+constexpr int kBcRows = 2;                                   // rows per thread
+constexpr int kBcCtaRows = (kBcThreads / 32) * kBcRows;      // rows per CTA of one (chunk, group)
+constexpr int kBcParts = kTR / kBcCtaRows;                   // CTAs per (chunk, group)
+static_assert(kBcParts * kBcCtaRows == kTR, "a chunk's rows split evenly over its CTAs");
+
+// conv + SiLU of one B/C value from its four pre-conv frames, oldest first
+__device__ __forceinline__ float bc_conv_silu(float4 w, float bias, float f0, float f1, float f2, float f3) {
+    float u = bias;
+    u = fmaf(w.x, f0, u);
+    u = fmaf(w.y, f1, u);
+    u = fmaf(w.z, f2, u);
+    u = fmaf(w.w, f3, u);
+    return silu_fast(u);
+}
+
+// Stores row `row` of 8 channels [n0, n0+8) of the (B or C) operand tiles of
+// one (sequence, chunk, group): B~ as bf16 hi + lo, C~ as bf16 hi; zeros when
+// the row is not live (past the sequence end, or channels past N).
+__device__ __forceinline__ void bc_store_row(uint8_t* tiles, int row, int n0, int which, bool live,
+                                             const float (&out)[8]) {
+    uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
+    if (live) {
+        uint32_t hb[8], lb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            hb[j] = float_to_bf16_bits(out[j]);
+            lb[j] = float_to_bf16_bits(out[j] - bf16_bits_to_float(hb[j]));
+        }
+        hi = make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16), hb[6] | (hb[7] << 16));
+        lo = make_uint4(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16), lb[4] | (lb[5] << 16), lb[6] | (lb[7] << 16));
+    }
+    const uint32_t off = tc::sw128_off(row, n0, kTR);
+    if (which == 0) {
+        *reinterpret_cast<uint4*>(tiles + off) = hi;
+        *reinterpret_cast<uint4*>(tiles + kTileBytes + off) = lo;
+    } else {
+        *reinterpret_cast<uint4*>(tiles + 2 * kTileBytes + off) = hi;
+    }
+}
 
 template <typename TA>
 __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nchunks) {
     const Shape& s = a.s;
-    const int c = blockIdx.x >> 2, quarter = blockIdx.x & 3, g = blockIdx.y, b = blockIdx.z;
+    const int c = blockIdx.x / kBcParts, part = blockIdx.x % kBcParts, g = blockIdx.y, b = blockIdx.z;
     const int T = a.T, Q = a.chunk;
     const int c0 = c * Q;
     const long HP = s.HP(), GN = s.GN(), CH = s.CH();
     uint8_t* tiles = reinterpret_cast<uint8_t*>(a.ws) + (((size_t)b * nchunks + c) * s.G + g) * 3 * kTileBytes;
-    uint8_t* tBh = tiles;
-    uint8_t* tBl = tiles + kTileBytes;
-    uint8_t* tCh = tiles + 2 * kTileBytes;
 
-    // 32 columns of 8 channels (16 for B, 16 for C) x 8 groups of 4 rows.
+    // 32 columns of 8 channels (16 for B, 16 for C) x (threads / 32) groups of kBcRows rows.
     const int cc = threadIdx.x & 31, rs = threadIdx.x >> 5;
     const int which = cc >> 4;  // 0: B, 1: C
     const int n0 = (cc & 15) * 8;
-    const int r0 = quarter * 32 + rs * kBcRows;
+    const int r0 = part * kBcCtaRows + rs * kBcRows;
     const bool real = n0 < s.N;
     const long ch0 = HP + which * GN + (long)g * s.N + n0;  // conv channel of n0
     const void* src = which ? a.C : a.B;
-    pdl_wait();  // B, C and the lengths may come from the previous kernel
+    pdl_wait();     // B, C and the lengths may come from the previous kernel
+    pdl_trigger();  // the SSD kernel may launch: its early reads are of data written before this kernel
     const int L = min(Q, seq_len(a, b) - c0);  // rows of this chunk in the sequence
     if (L <= 0) return;                        // past the sequence end: no tile is read
 
-    float out[kBcRows][8];
-    if (real && r0 < L) {
-        // pre-conv rows r0-3 .. r0+3, weights and bias: all loads issued before any use
-        float win[kBcRows + 3][8];
+    // pre-conv rows r0-3 .. r0+kBcRows-1, weights and bias: every load is
+    // issued before any use, so all are in flight together. A row outside the
+    // sequence (and not in the initial tail) reads the chunk's first row, a
+    // valid address, and counts as zero.
+    Act8<TA> v[kBcRows + 3];
+    bool have[kBcRows + 3];
+    float4 w[8], b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
+    const bool any = real && r0 < L;
+    if (any) {
 #pragma unroll
         for (int k = 0; k < kBcRows + 3; ++k) {
             const int t = c0 + r0 - 3 + k;
-            Act8<TA> v;
-            bool have = true;
-            if (t >= 0 && t < c0 + L)
-                v.load(src, (((size_t)b * T + t) * s.G + g) * s.N + n0);
-            else if (t < 0 && a.init_conv)
-                v.load(a.init_conv, ((size_t)b * (s.K - 1) + (s.K - 1 + t)) * CH + ch0);
-            else
-                have = false;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) win[k][j] = have ? v.get(j) : 0.f;
+            const bool in_seq = t >= 0 && t < c0 + L;
+            const bool from_tail = t < 0 && a.init_conv != nullptr;
+            have[k] = in_seq || from_tail;
+            const void* base = from_tail ? a.init_conv : src;
+            const size_t elem = from_tail ? ((size_t)b * (s.K - 1) + (s.K - 1 + t)) * CH + ch0
+                                          : (((size_t)b * T + (in_seq ? t : c0)) * s.G + g) * s.N + n0;
+            v[k].load_pinned(base, elem);
         }
-        float4 w[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = __ldg(reinterpret_cast<const float4*>(a.conv_w) + ch0 + j);
-        const float4 b0 = __ldg(reinterpret_cast<const float4*>(a.conv_b + ch0));
-        const float4 b1 = __ldg(reinterpret_cast<const float4*>(a.conv_b + ch0) + 1);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float4 wj = w[j];
-            const float bj = j < 4 ? (&b0.x)[j] : (&b1.x)[j - 4];
-#pragma unroll
-            for (int r = 0; r < kBcRows; ++r) {
-                float u = bj;
-                u = fmaf(wj.x, win[r][j], u);
-                u = fmaf(wj.y, win[r + 1][j], u);
-                u = fmaf(wj.z, win[r + 2][j], u);
-                u = fmaf(wj.w, win[r + 3][j], u);
-                out[r][j] = silu_fast(u);
-            }
-        }
+        for (int j = 0; j < 8; ++j) w[j] = ldg_pinned_f4(reinterpret_cast<const float4*>(a.conv_w) + ch0 + j);
+        b0 = ldg_pinned_f4(reinterpret_cast<const float4*>(a.conv_b + ch0));
+        b1 = ldg_pinned_f4(reinterpret_cast<const float4*>(a.conv_b + ch0) + 1);
     }
 #pragma unroll
     for (int r = 0; r < kBcRows; ++r) {
-        const int row = r0 + r;
-        uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-        if (real && row < L) {
-            uint32_t hb[8], lb[8];
+        float out[8];
+        if (any) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                hb[j] = float_to_bf16_bits(out[r][j]);
-                lb[j] = float_to_bf16_bits(out[r][j] - bf16_bits_to_float(hb[j]));
+                float f[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) f[k] = have[r + k] ? v[r + k].get(j) : 0.f;
+                out[j] = bc_conv_silu(w[j], j < 4 ? (&b0.x)[j] : (&b1.x)[j - 4], f[0], f[1], f[2], f[3]);
             }
-            hi = make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16), hb[6] | (hb[7] << 16));
-            lo = make_uint4(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16), lb[4] | (lb[5] << 16), lb[6] | (lb[7] << 16));
         }
-        const uint32_t off = tc::sw128_off(row, n0, kTR);
-        if (which == 0) {
-            *reinterpret_cast<uint4*>(tBh + off) = hi;
-            *reinterpret_cast<uint4*>(tBl + off) = lo;
-        } else {
-            *reinterpret_cast<uint4*>(tCh + off) = hi;
-        }
+        bc_store_row(tiles, r0 + r, n0, which, real && r0 + r < L, out);
     }
-    pdl_trigger();  // at the end, so waiting SSD CTAs do not crowd this grid off the SMs
 }
 
 // The final conv tail of 8 channels [c, c+8) of sequence b: frames Tb-3..Tb-1
@@ -146,30 +166,28 @@ __device__ void write_tail(const ScanArgs& a, int b, long c) {
     const Shape& s = a.s;
     const long CH = s.CH(), HP = s.HP(), GN = s.GN();
     const int T = a.T, Tb = seq_len(a, b);
+    // source of each frame chosen first, so the three loads go out together
     Act8<TA> vals[3];
-    bool zero[3];
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
         const int t = Tb - 3 + k;
-        zero[k] = false;
+        const void* base;
+        size_t elem;
         if (t >= 0) {
-            if (c < HP)
-                vals[k].load(a.x, ((size_t)b * T + t) * HP + c);
-            else if (c < HP + GN)
-                vals[k].load(a.B, ((size_t)b * T + t) * GN + (c - HP));
-            else
-                vals[k].load(a.C, ((size_t)b * T + t) * GN + (c - HP - GN));
-        } else if (a.init_conv) {
-            vals[k].load_rw(a.init_conv, ((size_t)b * 3 + (3 + t)) * CH + c);
+            base = c < HP ? a.x : (c < HP + GN ? a.B : a.C);
+            elem = c < HP ? ((size_t)b * T + t) * HP + c
+                          : ((size_t)b * T + t) * GN + (c < HP + GN ? c - HP : c - HP - GN);
         } else {
-            zero[k] = true;
+            base = a.init_conv;
+            elem = ((size_t)b * 3 + (3 + t)) * CH + c;
         }
+        if (base)
+            vals[k].load_rw(base, elem);
+        else
+            memset(&vals[k], 0, sizeof(vals[k]));
     }
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        if (zero[k]) memset(&vals[k], 0, sizeof(vals[k]));
-        vals[k].store(a.final_conv, ((size_t)b * 3 + k) * CH + c);
-    }
+    for (int k = 0; k < 3; ++k) vals[k].store(a.final_conv, ((size_t)b * 3 + k) * CH + c);
 }
 
 // ----------------------------------------------------------------- kernel 2
@@ -257,9 +275,6 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     const int h = blockIdx.x, b = blockIdx.y;
     const int g = h / (s.H / s.G);
     const int T = a.T, Q = a.chunk;
-    // this sequence's frames and chunks (the workspace is laid out for nchunks)
-    const int Tb = seq_len(a, b);
-    const int nchb = (Tb + Q - 1) / Q;
     const long HP = s.HP();
     const int tid = threadIdx.x, row = tid & 127, half = (tid >> 7) & 1, warp = tid >> 5, lane = tid & 31;
     const bool compute = tid < kComputeThreads;
@@ -293,6 +308,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         return false;
     };
 
+    // setup that reads no input: barriers, TMEM
     if (tid == kCtrl) {
         for (int i = 0; i < 6; ++i) tc::mbar_init(bar_a + i, 1);
         tc::mbar_init(bar_op1, kComputeThreads);
@@ -304,13 +320,40 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         tc::tmem_alloc(sTmem, kTmemCols);
         tc::tmem_relinquish();
     }
-    for (int i = tid; i < P; i += kSsdThreads) {
-        reinterpret_cast<float4*>(sCw)[i] = __ldg(reinterpret_cast<const float4*>(a.conv_w) + (long)h * P + i);
-        sCb[i] = __ldg(a.conv_b + (long)h * P + i);
+    // Every input read before the control thread's wait for the prologue's
+    // tiles was written before the prologue kernel started: this launch
+    // directly follows it, and may start early only once each prologue CTA has
+    // passed its own wait for its predecessor.
+
+    // this sequence's frames and chunks (the workspace is laid out for nchunks)
+    const int Tb = seq_len(a, b);
+    const int nchb = (Tb + Q - 1) / Q;
+    // the first chunk's x rows (the barrier is the control thread's own; the
+    // other threads wait on it only after the block sync)
+    if (tid == kCtrl && nchb > 0) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, 0);
+    // The other global loads of the setup, issued before any is used so that
+    // all are in flight together: this head's conv weights, its scalars, and
+    // dt_raw of this thread's row of the first chunk (kept raw, hence no stall
+    // before the block sync; from then on dt_raw is loaded one chunk ahead of
+    // the dt phase that uses it).
+    static_assert(P <= kSsdThreads, "one conv weight row per thread");
+    float4 cw = make_float4(0.f, 0.f, 0.f, 0.f);
+    float cb = 0.f;
+    if (tid < P) {
+        cw = ldg_pinned_f4(reinterpret_cast<const float4*>(a.conv_w) + (long)h * P + tid);
+        cb = ldg_pinned_f32(a.conv_b + (long)h * P + tid);
     }
-    const float A = -expf(__ldg(a.A_log + h));
-    const float Dh = __ldg(a.D + h);
-    const float dtb = __ldg(a.dt_bias + h);
+    const float A_log_h = ldg_pinned_f32(a.A_log + h);
+    const float Dh = ldg_pinned_f32(a.D + h);
+    const float dtb = ldg_pinned_f32(a.dt_bias + h);
+    ActRaw<TA> dt_raw_bits = 0;
+    if (compute && nchb > 0 && half == 0 && row < min(Q, Tb))
+        dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + row) * s.H + h);
+    if (tid < P) {
+        reinterpret_cast<float4*>(sCw)[tid] = cw;
+        sCb[tid] = cb;
+    }
+    const float A = -expf(A_log_h);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -323,8 +366,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     if (!compute) {
         // ================================================================ control
         if (tid == kCtrl && nchb > 0) {
-            stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, 0);  // x was written before the prologue kernel
-            pdl_wait();                                      // the operand tiles are its output
+            pdl_wait();  // the operand tiles are the prologue kernel's output
             const uint8_t* src = tiles_of(0);
             tc::mbar_arrive_expect_tx(bar_a, 2 * kTileBytes);
             tc::bulk_g2s(sm + L::kBh, src, kTileBytes, bar_a);
@@ -407,6 +449,30 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 }
             }
         }
+        __syncwarp();
+        // Final conv tail (the last K-1 pre-conv frames), written by this warp
+        // while the compute warps finish the last chunk's y. This CTA owns the
+        // tail of its head's x channels: their initial frames are read only by
+        // this CTA, in chunk 0, before the phase-1 handoff the loop above
+        // waited for. The first head of each group also owns the group's B and
+        // C channels, whose initial frames only the prologue kernel reads, and
+        // that kernel has finished once griddepcontrol.wait returns. So
+        // final_conv may alias init_conv.
+        pdl_wait();
+        const int R = s.H / s.G;
+        const int nx = P / 8, nbc = (h % R == 0) ? 2 * s.N / 8 : 0;
+        // (skipped if a wait gave up: chunk 0 may not have read the initial tail)
+        const int nt = *sFlag ? 0 : nx + nbc;
+        for (int v = lane; v < nt; v += 32) {
+            long ch;
+            if (v < nx)
+                ch = (long)h * P + v * 8;
+            else if (v - nx < s.N / 8)
+                ch = HP + (long)g * s.N + (v - nx) * 8;
+            else
+                ch = HP + s.GN() + (long)g * s.N + (v - nx - s.N / 8) * 8;
+            write_tail<TA>(a, b, ch);
+        }
     } else {
         // ================================================================ compute
         // initial state -> TMEM [n lanes][p columns]; rows n >= N stay zero
@@ -425,10 +491,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             }
             tc::tmem_wait_st();
         }
-        // dt_raw of this thread's row, loaded one chunk ahead of the dt phase that uses it
-        float dt_raw_next = 0.f;
-        if (nchb > 0 && half == 0 && row < min(Q, Tb))
-            dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + row) * s.H + h);
+        float dt_raw_next = raw_to_f32<TA>(dt_raw_bits);
 
         // dt = softplus(dt_raw + dt_bias), a = dt A, inclusive cumulative sum S over
         // a chunk of Lx rows, and the column factor of the decay mask,
@@ -712,24 +775,6 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                     a.final_ssm[(((size_t)b * s.H + h) * P + half * PH + q8 * 8 + q) * s.N + n] = v[q8][q];
         }
     }
-    // final conv tail (the last K-1 pre-conv frames). This CTA owns the tail of
-    // its head's x channels (whose initial frames only it has read); the first
-    // head of each group also owns the group's B and C channels (whose initial
-    // frames only the prologue kernel read). So in-place updates are safe.
-    {
-        const int R = s.H / s.G;
-        const int nx = P / 8, nbc = (h % R == 0) ? 2 * s.N / 8 : 0;
-        for (int v = tid; v < nx + nbc; v += kSsdThreads) {
-            long c;
-            if (v < nx)
-                c = (long)h * P + v * 8;
-            else if (v - nx < s.N / 8)
-                c = HP + (long)g * s.N + (v - nx) * 8;
-            else
-                c = HP + s.GN() + (long)g * s.N + (v - nx - s.N / 8) * 8;
-            write_tail<TA>(a, b, c);
-        }
-    }
     tc::tc_fence_before();
     __syncthreads();
     if (!compute) tc::tmem_dealloc(tm, kTmemCols);
@@ -805,7 +850,7 @@ template <typename TA>
 cudaError_t launch_bc_typed(const ScanArgs& a, cudaStream_t st) {
     const int nchunks = (a.T + a.chunk - 1) / a.chunk;
     if (nchunks == 0) return cudaSuccess;
-    return launch_pdl(scan_bc_kernel<TA>, dim3(nchunks * 4, a.s.G, a.batch), dim3(kBcThreads), 0, st, a, nchunks);
+    return launch_pdl(scan_bc_kernel<TA>, dim3(nchunks * kBcParts, a.s.G, a.batch), dim3(kBcThreads), 0, st, a, nchunks);
 }
 
 template <typename TA>
