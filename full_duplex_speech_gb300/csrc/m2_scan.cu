@@ -50,7 +50,7 @@ __device__ __forceinline__ int seq_len(const ScanArgs& a, int b) {
 // This kernel lets the SSD kernel launch as soon as every CTA here has passed its
 // griddepcontrol.wait: SSD CTAs then start at once on SMs without a CTA of
 // this kernel, and on each other SM as soon as its CTA here exits. (An SSD
-// CTA cannot share an SM with these CTAs: three of its nine warps, at 168
+// CTA cannot share an SM with these CTAs: three of its nine warps, at 160
 // registers, nearly fill one sub-partition's register file.) Two rows per
 // thread keep each CTA short.
 constexpr int kBcThreads = 256;
@@ -475,8 +475,13 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         }
     } else {
         // ================================================================ compute
-        // initial state -> TMEM [n lanes][p columns]; rows n >= N stay zero
-        {
+        // Initial state -> TMEM [n lanes][p columns]; rows n >= N stay zero.
+        // Without one (a fresh sequence) the first chunk's state step takes the
+        // old state as zero instead of reading TMEM, so nothing is stored here:
+        // TMEM stores right after the allocation were measured to take ~1 us.
+        // With no chunk at all the final state is read back from here.
+        const bool state_in_tmem = a.init_ssm != nullptr || nchb == 0;
+        if (state_in_tmem) {
             const int n = row;
 #pragma unroll
             for (int q8 = 0; q8 < NQ; ++q8) {
@@ -643,9 +648,17 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 const float decay = __expf(Slast);
                 const int n = row;
                 float v[NQ][8];
+                if (c > 0 || state_in_tmem) {
 #pragma unroll
-                for (int q8 = 0; q8 < NQ; ++q8) tc::tmem_ld8(tm + lane_base + kColState + half * PH + q8 * 8, v[q8]);
-                tc::tmem_wait_ld();
+                    for (int q8 = 0; q8 < NQ; ++q8)
+                        tc::tmem_ld8(tm + lane_base + kColState + half * PH + q8 * 8, v[q8]);
+                    tc::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int q8 = 0; q8 < NQ; ++q8)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) v[q8][q] = 0.f;
+                }
 #pragma unroll
                 for (int q8 = 0; q8 < NQ; ++q8) {
                     const int p0 = half * PH + q8 * 8;
