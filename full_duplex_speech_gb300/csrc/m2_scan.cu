@@ -335,7 +335,8 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     // all are in flight together: this head's conv weights, its scalars, and
     // dt_raw of this thread's row of the first chunk (kept raw, hence no stall
     // before the block sync; from then on dt_raw is loaded one chunk ahead of
-    // the dt phase that uses it).
+    // the dt phase that uses it, and kept raw until then, so that its latency
+    // passes under the wait for the chunk's MMAs).
     static_assert(P <= kSsdThreads, "one conv weight row per thread");
     float4 cw = make_float4(0.f, 0.f, 0.f, 0.f);
     float cb = 0.f;
@@ -496,7 +497,6 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             }
             tc::tmem_wait_st();
         }
-        float dt_raw_next = raw_to_f32<TA>(dt_raw_bits);
 
         // dt = softplus(dt_raw + dt_bias), a = dt A, inclusive cumulative sum S over
         // a chunk of Lx rows, and the column factor of the decay mask,
@@ -562,10 +562,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         };
 
         if (nchb > 0) {
-            dt_phase(min(Q, Tb), dt_raw_next);
-            dt_raw_next = 0.f;
+            dt_phase(min(Q, Tb), raw_to_f32<TA>(dt_raw_bits));
+            dt_raw_bits = 0;
             if (half == 0 && nchb > 1 && row < min(Q, Tb - Q))
-                dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + Q + row) * s.H + h);
+                dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + Q + row) * s.H + h);
         }
 
         // The chunk loop is skewed so that CUDA-core work overlaps the tensor
@@ -752,10 +752,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             // 6. meanwhile: the next chunk's dt phase (the mask above was the last
             //    reader of this chunk's S, dt and Eb; S_i is kept in a register)
             if (has_next) {
-                dt_phase(Ln, dt_raw_next);
-                dt_raw_next = 0.f;
+                dt_phase(Ln, raw_to_f32<TA>(dt_raw_bits));
+                dt_raw_bits = 0;
                 if (half == 0 && row < Lnn)
-                    dt_raw_next = load_act<TA>(a.dt_raw, ((size_t)b * T + c0 + 2 * Q + row) * s.H + h);
+                    dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + c0 + 2 * Q + row) * s.H + h);
             }
             wait_ok(bar_y, par, ERR_MBAR_TIMEOUT_MMA);
             tc::tc_fence_after();
