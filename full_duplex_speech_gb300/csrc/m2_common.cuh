@@ -141,9 +141,10 @@ __device__ __forceinline__ float softplus_f32(float z) {
 __device__ __forceinline__ float silu_f32(float u) { return u / (1.f + expf(-u)); }
 
 // The same with the fast exponential and division intrinsics (relative error
-// ~1e-7 here). The exponent is capped at 80 so the divisor stays finite: for
-// u < -80 the result is below 1e-33 in magnitude either way.
-__device__ __forceinline__ float silu_fast(float u) { return __fdividef(u, 1.f + __expf(fminf(-u, 80.f))); }
+// ~1e-7 here). Where the divisor is huge (u below about -87) the fast
+// division returns 0 (its reciprocal of a value above 2^126, or of +inf, is
+// 0), where the exact result is below 1e-36 in magnitude.
+__device__ __forceinline__ float silu_fast(float u) { return __fdividef(u, 1.f + __expf(-u)); }
 
 // Programmatic dependent launch. A kernel launched with programmatic stream
 // serialization may start before its predecessor in the stream finishes;

@@ -255,3 +255,16 @@ def test_varlen_lengths_are_clamped(m2):
     y1, fs1, fc1 = gpu_scan_varlen(m2, d, inp, 16, [0, 40])
     for a_, b_ in ((y, y1), (fs, fs1), (fc, fc1)):
         np.testing.assert_array_equal(bits_of(a_), bits_of(b_))
+
+
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+def test_saturated_silu_channels(m2, act):
+    """Conv pre-activations far below zero (a bias of -300 on every other
+    channel of x, B and C) saturate SiLU to zero, as the oracle's exact
+    u / (1 + e^-u) does: no NaN or infinity from the overflowing exponential."""
+    d = Dims(H=8, P=32, N=64, G=2)
+    inp = mixer_inputs(900, d, 2, 150, act)
+    inp["conv_b"] = inp["conv_b"].copy()
+    inp["conv_b"][::2] = -300.0
+    y, fs, _ = check(m2, d, inp, 64, 2, 150)
+    assert np.isfinite(from_dev_act(y, act)).all() and np.isfinite(fs.cpu().numpy()).all()

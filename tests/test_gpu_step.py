@@ -155,3 +155,23 @@ def test_step_session_counts_real_shape(m2, S):
     assert state_error(ssm_dev.cpu().numpy(), ssm_ref) <= STATE_TOL
     exp_tail = _tail_bits(conv0, _frame(inp, 0), d)
     np.testing.assert_array_equal(bits_of(conv_dev), np.ascontiguousarray(exp_tail).view(np.uint8).reshape(-1))
+
+
+def test_step_saturated_silu_channels(m2):
+    """The step's conv + SiLU with pre-activations far below zero (bias -300 on
+    every other channel): SiLU saturates to zero as in the oracle."""
+    d, S, act = Dims(H=8, P=32, N=64, G=2), 3, "bf16"
+    inp = mixer_inputs(910, d, S, 1, act)
+    inp["conv_b"] = inp["conv_b"].copy()
+    inp["conv_b"][::2] = -300.0
+    ssm0 = ssm_state_inputs(911, d, S, scale=0.2)
+    conv0 = conv_state_inputs(912, d, S, act)
+    ssm_dev, conv_dev = to_dev(ssm0), to_dev(conv0)
+    y = _gpu_step(m2, d, S, _frame(inp, 0), _params_dev(inp), ssm_dev, conv_dev, act)
+    ssm_ref = ssm0.astype(np.float64).copy()
+    conv_ref = as_f64(conv0, act).copy()
+    import oracle
+    y_ref = oracle.mixer_step(d, _frame(inp, 0), inp, ssm_ref, conv_ref)
+    assert np.isfinite(from_dev_act(y, act)).all()
+    assert y_error(from_dev_act(y, act), y_ref, act) <= Y_TOL
+    assert state_error(ssm_dev.cpu().numpy(), ssm_ref) <= STATE_TOL
