@@ -201,13 +201,16 @@ constexpr int kCtrl = kComputeThreads;  // the control thread
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kRawRows = kTR + 3;  // pre-conv rows of one chunk plus the 3-frame halo
 // TMEM columns
-constexpr uint32_t kColG = 0, kColState = 128, kColYd = 256, kColYo = 384, kTmemCols = 512;
+// (M, the masked G in bf16, is the A operand of Y_diag straight from TMEM:
+// row i on lane i, two columns j per 32-bit TMEM column.)
+constexpr uint32_t kColG = 0, kColState = 128, kColYd = 224, kColYo = 320, kColM = 416, kTmemCols = 512;
+static_assert(kColYo + 80 <= kColM && kColM + kTR / 2 <= kTmemCols, "accumulators and M fit the allocation");
 
 template <typename TA, int P>
 struct SsdSmem {
     static constexpr uint32_t kC = 0;                     // C~ hi           (K-major SW128)
     static constexpr uint32_t kBh = kTileBytes;           // B~ hi           (K-major / MN-major SW128)
-    static constexpr uint32_t kBl = 2 * kTileBytes;       // B~ lo, then M   (SW128)
+    static constexpr uint32_t kBl = 2 * kTileBytes;       // B~ lo           (SW128)
     static constexpr uint32_t kPT = kTR * P * 2;          // one [128 x P] bf16 interleaved tile
     static constexpr uint32_t kX = 3 * kTileBytes;        // x~ hi           (MN-major interleave, K = j)
     static constexpr uint32_t kWh = kX + kPT;             // (w o x~) hi
@@ -291,7 +294,6 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     uint64_t* bar_b = bar_a + 1;                                   // B~ lo tile landed
     uint64_t* bar_x = bar_a + 2;                                   // pre-conv x rows landed
     uint64_t* bar_g = bar_a + 3;                                   // G done
-    uint64_t* bar_bl = bar_a + 4;                                  // state terms reading B~ lo done
     uint64_t* bar_y = bar_a + 5;                                   // every MMA of the chunk done
     uint64_t* bar_op1 = bar_a + 6;                                 // phase-1 operands written (256 arrivals)
     uint64_t* bar_op2 = bar_a + 7;                                 // phase-2 operands written (256 arrivals)
@@ -404,26 +406,21 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 if (has_next && ok1) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, c0 + Q);
                 const bool okb = wait_ok(bar_b, par, ERR_MBAR_TIMEOUT_LOAD);
                 if (ok1 && okt && okb) {
-                    // phase 1: the state terms that read B~ lo (commit), then the
-                    // rest of state += B~^T (w o x~)
-                    for (int ks = 0; ks < ksteps; ++ks)
-                        tc::mma_bf16(tm + kColState, tc::sdesc(sBl + ks * 2048, kPanel, 1024, 2),
-                                     tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
-                    tc::mma_commit(bar_bl);
+                    // phase 1: state += B~^T (w o x~) as hi*hi + hi*lo + lo*hi
                     for (int ks = 0; ks < ksteps; ++ks) {
                         const uint64_t dBh = tc::sdesc(sBh + ks * 2048, kPanel, 1024, 2);
-                        tc::mma_bf16(tm + kColState, dBh, tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
+                        const uint64_t dWh = tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0);
+                        tc::mma_bf16(tm + kColState, tc::sdesc(sBl + ks * 2048, kPanel, 1024, 2), dWh, idS, 1);
+                        tc::mma_bf16(tm + kColState, dBh, dWh, idS, 1);
                         tc::mma_bf16(tm + kColState, dBh, tc::sdesc(sWl + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
                     }
                 }
                 if (wait_ok(bar_op2, par, ERR_MBAR_TIMEOUT_MMA)) {
                     tc::tc_fence_after();
-                    // phase 2: Y_diag += M x~ (onto D x~) and Y_off = C~ h_prev^T
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
-                        tc::mma_bf16(tm + kColYd, tc::sdesc(sBl + koff, 0, 1024, 2),
-                                     tc::sdesc(sX + ks * 2 * LBO_I, LBO_I, 128, 0), idY, 1);
-                    }
+                    // phase 2: Y_diag += M x~ (onto D x~, M from TMEM) and Y_off = C~ h_prev^T
+                    for (int ks = 0; ks < ksteps; ++ks)
+                        tc::mma_bf16_tmem_a(tm + kColYd, tm + kColM + ks * 8,
+                                            tc::sdesc(sX + ks * 2 * LBO_I, LBO_I, 128, 0), idY, 1);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
@@ -691,11 +688,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 tc::tmem_wait_st();
             }
             wait_ok(bar_g, par, ERR_MBAR_TIMEOUT_MMA);
-            wait_ok(bar_bl, par, ERR_MBAR_TIMEOUT_MMA);
             tc::tc_fence_after();
 
-            // 5. M = G o exp(S_i - S_j) dt_j (j <= i) -> bf16, K-major SW128 over the B~ lo
-            //    tile (its readers are done; the remaining state MMAs run meanwhile).
+            // 5. M = G o exp(S_i - S_j) dt_j (j <= i) -> bf16 into TMEM, the A
+            //    operand of Y_diag (the state MMAs run meanwhile).
             //    An 8-column block [j0, j1] wholly left of row i factors as
             //    exp(S_i - S_j1) * Eb_j, both factors <= 1 (S does not increase);
             //    the block holding the diagonal takes one exponential per entry.
@@ -738,14 +734,15 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                         pk[e8 / 2 + 2] = pack2(m[4], m[5]);
                         pk[e8 / 2 + 3] = pack2(m[6], m[7]);
                     }
-                    *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0, kTR)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4*>(sm + L::kBl + tc::sw128_off(i, j0 + 8, kTR)) =
-                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    // columns j0 .. j0+15 of row i: 8 TMEM columns
+                    float mv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mv[e] = __uint_as_float(pk[e]);
+                    tc::tmem_st8(tm + lane_base + kColM + j0 / 2, mv);
                 }
+                tc::tmem_wait_st();
             }
-            // hand the phase-2 operands (M tile, D x~ in Y_diag) to the control warp
-            tc::fence_proxy_async_smem();
+            // hand the phase-2 operands (M and D x~ in TMEM) to the control warp
             tc::tc_fence_before();
             tc::mbar_arrive(bar_op2);
 
