@@ -201,10 +201,14 @@ constexpr int kCtrl = kComputeThreads;  // the control thread
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kRawRows = kTR + 3;  // pre-conv rows of one chunk plus the 3-frame halo
 // TMEM columns
-// (M, the masked G in bf16, is the A operand of Y_diag straight from TMEM:
-// row i on lane i, two columns j per 32-bit TMEM column.)
-constexpr uint32_t kColG = 0, kColState = 128, kColYd = 224, kColYo = 320, kColM = 416, kTmemCols = 512;
-static_assert(kColYo + 80 <= kColM && kColM + kTR / 2 <= kTmemCols, "accumulators and M fit the allocation");
+// M, the masked G in bf16, is the A operand of Y_diag straight from TMEM:
+// row i on lane i, two columns j per 32-bit TMEM column. Each half of the
+// compute warps writes its 64 columns j of M over the first 32 of the 64 G
+// columns it has just read (so M for j = 64h + k sits at column 64h + k/2).
+// Y_off is double-buffered by chunk parity: a chunk's Y_off MMAs run while
+// the previous chunk's y is still being read.
+constexpr uint32_t kColG = 0, kColState = 128, kColYd = 224, kColYo0 = 320, kColYo1 = 416, kTmemCols = 512;
+static_assert(kColYo1 + 80 <= kTmemCols, "accumulators of up to 80 columns fit the allocation");
 
 template <typename TA, int P>
 struct SsdSmem {
@@ -294,6 +298,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     uint64_t* bar_b = bar_a + 1;                                   // B~ lo tile landed
     uint64_t* bar_x = bar_a + 2;                                   // pre-conv x rows landed
     uint64_t* bar_g = bar_a + 3;                                   // G done
+    uint64_t* bar_op0 = bar_a + 4;                                 // h_prev tile written (256 arrivals)
     uint64_t* bar_y = bar_a + 5;                                   // every MMA of the chunk done
     uint64_t* bar_op1 = bar_a + 6;                                 // phase-1 operands written (256 arrivals)
     uint64_t* bar_op2 = bar_a + 7;                                 // phase-2 operands written (256 arrivals)
@@ -312,7 +317,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
 
     // setup that reads no input: barriers, TMEM
     if (tid == kCtrl) {
-        for (int i = 0; i < 6; ++i) tc::mbar_init(bar_a + i, 1);
+        for (int i = 0; i < 4; ++i) tc::mbar_init(bar_a + i, 1);
+        tc::mbar_init(bar_op0, kComputeThreads);
+        tc::mbar_init(bar_y, 1);
         tc::mbar_init(bar_op1, kComputeThreads);
         tc::mbar_init(bar_op2, kComputeThreads);
         tc::fence_mbar_init();
@@ -387,8 +394,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 const uint32_t par = c & 1;
                 const bool has_next = c + 1 < nchb;
                 // G = C~ B~^T as soon as the tiles are in: it needs nothing from the
-                // compute warps, and its TMEM columns were last read by the previous
-                // chunk's mask (before that chunk's phase-2 handoff)
+                // compute warps, and its TMEM columns (which also held the previous
+                // chunk's M) were last read by the previous chunk's Y_diag MMAs,
+                // done before these tiles were fetched
                 const bool okt = wait_ok(bar_a, par, ERR_MBAR_TIMEOUT_LOAD);
                 if (okt) {
                     tc::tc_fence_after();
@@ -400,33 +408,47 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                     }
                     tc::mma_commit(bar_g);
                 }
+                // Y_off = C~ h_prev^T as soon as the h_prev tile is written: it runs
+                // under the compute warps' conv (into the Y_off buffer of this
+                // chunk's parity; the other one holds the previous chunk's, still
+                // to be read)
+                const bool ok0 = wait_ok(bar_op0, par, ERR_MBAR_TIMEOUT_MMA);
+                tc::tc_fence_after();
+                const uint32_t colYo = par ? kColYo1 : kColYo0;
+                if (ok0 && okt) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
+                        tc::mma_bf16(tm + colYo, tc::sdesc(sC + koff, 0, 1024, 2),
+                                     tc::sdesc(sH + ks * 2 * LBO_I, LBO_I, 128, 0), idY, ks > 0);
+                    }
+                }
                 const bool ok1 = wait_ok(bar_op1, par, ERR_MBAR_TIMEOUT_MMA);
                 tc::tc_fence_after();
-                // the staged rows are consumed: stage the next chunk's
-                if (has_next && ok1) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, c0 + Q);
                 const bool okb = wait_ok(bar_b, par, ERR_MBAR_TIMEOUT_LOAD);
-                if (ok1 && okt && okb) {
-                    // phase 1: state += B~^T (w o x~) as hi*hi + hi*lo + lo*hi
+                if (ok0 && ok1 && okt && okb) {
+                    // phase 1: state += B~^T (w o x~) as hi*hi + hi*lo + lo*hi. A
+                    // fresh sequence's state is not in TMEM before its first chunk:
+                    // that chunk's first product overwrites the accumulator.
+                    const uint32_t acc0 = (c > 0 || a.init_ssm != nullptr) ? 1u : 0u;
                     for (int ks = 0; ks < ksteps; ++ks) {
                         const uint64_t dBh = tc::sdesc(sBh + ks * 2048, kPanel, 1024, 2);
                         const uint64_t dWh = tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0);
-                        tc::mma_bf16(tm + kColState, tc::sdesc(sBl + ks * 2048, kPanel, 1024, 2), dWh, idS, 1);
+                        tc::mma_bf16(tm + kColState, tc::sdesc(sBl + ks * 2048, kPanel, 1024, 2), dWh, idS,
+                                     ks > 0 ? 1u : acc0);
                         tc::mma_bf16(tm + kColState, dBh, dWh, idS, 1);
                         tc::mma_bf16(tm + kColState, dBh, tc::sdesc(sWl + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
                     }
                 }
+                // the staged rows are consumed: stage the next chunk's (needed only
+                // at the next chunk's conv, so after this chunk's MMAs are queued)
+                if (has_next && ok1) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, c0 + Q);
                 if (wait_ok(bar_op2, par, ERR_MBAR_TIMEOUT_MMA)) {
                     tc::tc_fence_after();
-                    // phase 2: Y_diag += M x~ (onto D x~, M from TMEM) and Y_off = C~ h_prev^T
+                    // phase 2: Y_diag += M x~ (onto D x~, M from TMEM)
                     for (int ks = 0; ks < ksteps; ++ks)
-                        tc::mma_bf16_tmem_a(tm + kColYd, tm + kColM + ks * 8,
+                        tc::mma_bf16_tmem_a(tm + kColYd, tm + kColG + (ks >> 2) * 64 + (ks & 3) * 8,
                                             tc::sdesc(sX + ks * 2 * LBO_I, LBO_I, 128, 0), idY, 1);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
-                        tc::mma_bf16(tm + kColYo, tc::sdesc(sC + koff, 0, 1024, 2),
-                                     tc::sdesc(sH + ks * 2 * LBO_I, LBO_I, 128, 0), idY, ks > 0);
-                    }
                     tc::mma_commit(bar_y);
                 }
                 // every operand tile of this chunk is consumed: fetch the next chunk's
@@ -528,14 +550,14 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         // y = (D x~ + M x~) + exp(S_i) Y_off for the chunk whose results sit in TMEM.
         // The TMEM loads are warp-collective (.sync.aligned): every lane issues
         // them; only the stores are predicated.
-        auto y_epilogue = [&](int c0y, int Ly, float eSy) {
+        auto y_epilogue = [&](int c0y, int Ly, float eSy, uint32_t colYo) {
             const bool live = row < Ly;
             const size_t ybase = (((size_t)b * T + c0y + row) * s.H + h) * P;
             float yd[NQ][8], yo[NQ][8];
 #pragma unroll
             for (int q8 = 0; q8 < NQ; ++q8) {
                 tc::tmem_ld8(tm + lane_base + kColYd + half * PH + q8 * 8, yd[q8]);
-                tc::tmem_ld8(tm + lane_base + kColYo + half * PH + q8 * 8, yo[q8]);
+                tc::tmem_ld8(tm + lane_base + colYo + half * PH + q8 * 8, yo[q8]);
             }
             tc::tmem_wait_ld();
 #pragma unroll
@@ -578,7 +600,48 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             const int Ln = has_next ? min(Q, Tb - c0 - Q) : 0;
             const int Lnn = c + 2 < nchb ? min(Q, Tb - c0 - 2 * Q) : 0;
 
-            // 1. this chunk's staged x rows (its dt phase ran one step earlier)
+            // 1. state: h_prev (bf16) into shared memory for Y_off, then
+            //    h <- exp(S_last) h in TMEM (its dt phase ran one step earlier;
+            //    the previous chunk's MMAs are done). A fresh sequence's first
+            //    chunk has h_prev = 0 and leaves TMEM alone: the first state MMA
+            //    overwrites the accumulator.
+            const float Slast = sS[Lc - 1];
+            {
+                const float decay = __expf(Slast);
+                const int n = row;
+                const bool in_tmem = c > 0 || state_in_tmem;
+                float v[NQ][8];
+                if (in_tmem) {
+#pragma unroll
+                    for (int q8 = 0; q8 < NQ; ++q8)
+                        tc::tmem_ld8(tm + lane_base + kColState + half * PH + q8 * 8, v[q8]);
+                    tc::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int q8 = 0; q8 < NQ; ++q8)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) v[q8][q] = 0.f;
+                }
+#pragma unroll
+                for (int q8 = 0; q8 < NQ; ++q8) {
+                    const int p0 = half * PH + q8 * 8;
+                    *reinterpret_cast<uint4*>(sm + L::kH + tc::mn_inter_off(p0, n, P)) =
+                        make_uint4(pack2(v[q8][0], v[q8][1]), pack2(v[q8][2], v[q8][3]), pack2(v[q8][4], v[q8][5]),
+                                   pack2(v[q8][6], v[q8][7]));
+                    if (in_tmem) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) v[q8][q] *= decay;
+                        tc::tmem_st8(tm + lane_base + kColState + p0, v[q8]);
+                    }
+                }
+                if (in_tmem) tc::tmem_wait_st();
+            }
+            // hand the h_prev tile (and the scaled state) to the control warp
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::mbar_arrive(bar_op0);
+
+            // 2a. this chunk's staged x rows
             wait_ok(bar_x, par, ERR_MBAR_TIMEOUT_LOAD);
             compute_sync();
             if (c == 0 && a.init_conv) {
@@ -593,7 +656,6 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 }
                 compute_sync();
             }
-            const float Slast = sS[Lc - 1];
             const float Si = sS[row];
             const float wi = row < Lc ? __expf(Slast - Si) * sDt[row] : 0.f;
 
@@ -640,43 +702,15 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 *reinterpret_cast<uint4*>(sm + L::kWl + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
             }
 
-            // 3. state: h_prev (bf16) into shared memory for Y_off, then h <- exp(S_last) h in TMEM
-            {
-                const float decay = __expf(Slast);
-                const int n = row;
-                float v[NQ][8];
-                if (c > 0 || state_in_tmem) {
-#pragma unroll
-                    for (int q8 = 0; q8 < NQ; ++q8)
-                        tc::tmem_ld8(tm + lane_base + kColState + half * PH + q8 * 8, v[q8]);
-                    tc::tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int q8 = 0; q8 < NQ; ++q8)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) v[q8][q] = 0.f;
-                }
-#pragma unroll
-                for (int q8 = 0; q8 < NQ; ++q8) {
-                    const int p0 = half * PH + q8 * 8;
-                    *reinterpret_cast<uint4*>(sm + L::kH + tc::mn_inter_off(p0, n, P)) =
-                        make_uint4(pack2(v[q8][0], v[q8][1]), pack2(v[q8][2], v[q8][3]), pack2(v[q8][4], v[q8][5]),
-                                   pack2(v[q8][6], v[q8][7]));
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) v[q8][q] *= decay;
-                    tc::tmem_st8(tm + lane_base + kColState + p0, v[q8]);
-                }
-                tc::tmem_wait_st();
-            }
-            // hand the phase-1 operands (x~, w o x~ tiles, h tile, scaled state) to the control warp
+            // hand the phase-1 operands (x~ and w o x~ tiles) to the control warp
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
             tc::mbar_arrive(bar_op1);
 
-            // 4. meanwhile: the previous chunk's y (phase 1 writes only the G and
-            //    state columns), then this chunk's D x~ preloaded into the Y_diag
-            //    accumulator that phase 2 adds M x~ onto
-            if (c > 0) y_epilogue(c0_prev, L_prev, eS_prev);
+            // 4. meanwhile: the previous chunk's y (this chunk's MMAs so far write
+            //    G, the state and the other Y_off buffer), then this chunk's D x~
+            //    preloaded into the Y_diag accumulator that phase 2 adds M x~ onto
+            if (c > 0) y_epilogue(c0_prev, L_prev, eS_prev, par ? kColYo0 : kColYo1);
             {
                 float dx[8];
 #pragma unroll
@@ -734,11 +768,12 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                         pk[e8 / 2 + 2] = pack2(m[4], m[5]);
                         pk[e8 / 2 + 3] = pack2(m[6], m[7]);
                     }
-                    // columns j0 .. j0+15 of row i: 8 TMEM columns
+                    // columns j0 .. j0+15 of row i: 8 TMEM columns over G columns
+                    // this thread has read (all of them are in gv)
                     float mv[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) mv[e] = __uint_as_float(pk[e]);
-                    tc::tmem_st8(tm + lane_base + kColM + j0 / 2, mv);
+                    tc::tmem_st8(tm + lane_base + kColG + half * 64 + q * 8, mv);
                 }
                 tc::tmem_wait_st();
             }
@@ -762,7 +797,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         }
         // the last chunk's y
         compute_sync();
-        if (!*sFlag && nchb > 0) y_epilogue(c0_prev, L_prev, eS_prev);
+        if (!*sFlag && nchb > 0) y_epilogue(c0_prev, L_prev, eS_prev, ((nchb - 1) & 1) ? kColYo1 : kColYo0);
     }
 
     pdl_trigger();
