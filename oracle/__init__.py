@@ -67,8 +67,9 @@ def _load():
             lib.m2o_mixer_scan.argtypes = [ctypes.POINTER(_Dims)] + [dp] * 14 + [ip] * 4
             lib.m2o_mixer_step.argtypes = [ctypes.POINTER(_Dims), ip] + [dp] * 12 + [ip]
             lib.m2o_gated_norm.argtypes = [ip, ip, ip, dp, dp, dp, ctypes.c_double, dp]
+            lib.m2o_qlinear.argtypes = [ip, ip, ip, ip, ctypes.POINTER(ctypes.c_uint32), dp, dp, dp, dp]
             for f in ("m2o_ssm", "m2o_conv_silu", "m2o_conv_tail", "m2o_mixer_scan", "m2o_mixer_step",
-                      "m2o_gated_norm"):
+                      "m2o_gated_norm", "m2o_qlinear"):
                 getattr(lib, f).restype = ip
             _lib = lib
     return _lib
@@ -199,3 +200,20 @@ def gated_norm(y, z, weight, groups: int, eps: float = 1e-5) -> np.ndarray:
                                 _ptr(out))
     _check(rc, "gated_norm")
     return out
+
+
+def qlinear(x, wq, scales, biases, group: int = 64) -> np.ndarray:
+    """Affine group-quantized linear layer. x [..., in] (values as fp64);
+    wq [out, in/8] uint32 (eight 4-bit fields per word, the first input in
+    the lowest bits); scales, biases [out, in/group]. Returns y [..., out]
+    in fp64 (W[o][i] = scale * q + bias per group of `group` inputs)."""
+    x = _f64(x)
+    wq = np.ascontiguousarray(wq, dtype=np.uint32)
+    n_out, in_features = wq.shape[0], wq.shape[1] * 8
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    y = np.empty(x.shape[:-1] + (n_out,), dtype=np.float64)
+    rc = _load().m2o_qlinear(rows, in_features, n_out, int(group),
+                             wq.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), _ptr(_f64(scales)),
+                             _ptr(_f64(biases)), _ptr(x), _ptr(y))
+    _check(rc, "qlinear")
+    return y

@@ -35,6 +35,7 @@
  *   channel c: x at c = h*P+p, B at H*P + g*N+n, C at H*P + G*N + g*N+n.
  */
 #include <math.h>
+#include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -368,5 +369,33 @@ int m2o_gated_norm(int rows, int width, int groups, const double* y, const doubl
         }
     }
     free(v);
+    return M2O_OK;
+}
+
+/* Affine group-quantized linear layer: the mixer's input and output
+ * projections, which the VoiceChat 4-bit checkpoint stores quantized with
+ * group_size 64 and bits 4 (Nemotron VoiceChat page, config.json,
+ * `quantization`). Weight element (o, i) is the 4-bit field q = bits
+ * 4*(i%8) .. 4*(i%8)+3 of the 32-bit word wq[o][i/8] (the first element in
+ * the lowest bits), dequantized per group of `group` consecutive inputs:
+ *     W[o][i] = scale[o][i/group] * q + bias[o][i/group]
+ *     y[r][o] = sum_i W[o][i] x[r][i]
+ * x [rows, in]; y [rows, out]; scale, bias [out, in/group]. */
+int m2o_qlinear(int rows, int in, int out, int group, const uint32_t* wq, const double* scale,
+                const double* bias, const double* x, double* y) {
+    if (rows < 0 || in <= 0 || out <= 0 || group <= 0 || in % group != 0 || in % 8 != 0 || !wq || !scale ||
+        !bias || !x || !y)
+        return M2O_EINVAL;
+    const int ngroups = in / group;
+    for (long r = 0; r < rows; ++r)
+        for (int o = 0; o < out; ++o) y[r * out + o] = 0.0;
+    for (int o = 0; o < out; ++o) {
+        for (int i = 0; i < in; ++i) {
+            const uint32_t word = wq[(long)o * (in / 8) + i / 8];
+            const int q = (int)((word >> (4 * (i % 8))) & 15u);
+            const double w = scale[(long)o * ngroups + i / group] * q + bias[(long)o * ngroups + i / group];
+            for (long r = 0; r < rows; ++r) y[r * out + o] += w * x[r * in + i];
+        }
+    }
     return M2O_OK;
 }

@@ -220,3 +220,19 @@ def norm_inputs(seed: int, d: Dims, rows: int, act: str = "bf16") -> dict:
     if act == "bf16":
         y, z = f32_to_bf16_bits(y), f32_to_bf16_bits(z)
     return dict(y=y, z=z, weight=w, act=act)
+
+
+def qlinear_inputs(seed: int, rows: int, in_features: int, out_features: int, group: int = 64) -> dict:
+    """Inputs of a 4-bit affine group-quantized linear layer: x [rows, in]
+    ~ N(0, 1) as bf16 bit patterns; wq [out, in/8] uint32 of uniformly drawn
+    4-bit fields; scales ~ U(0.5, 1.5) / (4 sqrt(in)) and biases
+    ~ -7.5 scale U(0.8, 1.2) [out, in/group] as bf16 bit patterns, so the
+    weights are centred near zero with a spread like a trained layer's."""
+    rng = np.random.default_rng([seed, 0x5EED, 6])
+    x = rng.standard_normal((rows, in_features), dtype=np.float32)
+    wq = rng.integers(0, 2**32, size=(out_features, in_features // 8), dtype=np.uint64).astype(np.uint32)
+    ng = in_features // group
+    scales = rng.uniform(0.5, 1.5, size=(out_features, ng)) / (4.0 * np.sqrt(in_features))
+    biases = -7.5 * scales * rng.uniform(0.8, 1.2, size=(out_features, ng))
+    return dict(x=f32_to_bf16_bits(x), wq=wq, scales=f32_to_bf16_bits(scales.astype(np.float32)),
+                biases=f32_to_bf16_bits(biases.astype(np.float32)), group=group)

@@ -403,3 +403,52 @@ def test_gated_norm_gate_and_invariances():
     # each group has mean square (weight-free) 1
     unit = oracle.gated_norm(y, z, np.ones(width), groups, 0.0).reshape(rows, groups, -1)
     np.testing.assert_allclose(np.mean(unit ** 2, axis=-1), 1.0, rtol=1e-12)
+
+
+# ------------------------------------------------ quantized mixer projections
+# Two output rows of 64 inputs, one group, written out by hand: row 0 holds
+# q = i % 16 (words 0x76543210, 0xFEDCBA98, ...: the first input in the lowest
+# four bits), row 1 holds q = 15 - i % 16.
+_QL_WQ = np.array([[0x76543210, 0xFEDCBA98] * 4, [0x89ABCDEF, 0x01234567] * 4], dtype=np.uint32)
+_QL_SCALE = np.array([[0.5], [2.0]])
+_QL_BIAS = np.array([[-4.0], [1.0]])
+
+
+def test_qlinear_worked_example():
+    """W0[i] = 0.5 (i % 16) - 4 and W1[i] = 2 (15 - i % 16) + 1, so with
+    x = 1: y0 = 64 (0.5 * 7.5 - 4) = -16 and y1 = 4 * sum_k (31 - 2k) = 1024;
+    unit vectors read single weights (i = 13: 2.5 and 5; i = 63: 3.5 and 1)."""
+    import oracle
+    np.testing.assert_array_equal(oracle.qlinear(np.ones(64), _QL_WQ, _QL_SCALE, _QL_BIAS), [-16.0, 1024.0])
+    for i, want in ((13, [2.5, 5.0]), (63, [3.5, 1.0]), (0, [-4.0, 31.0]), (8, [0.0, 15.0])):
+        e = np.zeros(64)
+        e[i] = 1.0
+        np.testing.assert_array_equal(oracle.qlinear(e, _QL_WQ, _QL_SCALE, _QL_BIAS), want)
+
+
+def test_qlinear_equals_dense_matmul():
+    """Against a library matmul (torch, fp64) of the weights decoded
+    separately with vectorised shifts, for several rows and groups."""
+    import oracle
+    from seeded_inputs import bf16_bits_to_f64, qlinear_inputs
+    inp = qlinear_inputs(7, 3, 256, 40)
+    x, s, b = (bf16_bits_to_f64(inp[k]) for k in ("x", "scales", "biases"))
+    q = (inp["wq"][:, :, None].astype(np.int64) >> (4 * np.arange(8))) & 15
+    w = np.repeat(s, 64, axis=1) * q.reshape(40, 256) + np.repeat(b, 64, axis=1)
+    ref = (torch.from_numpy(x) @ torch.from_numpy(w).T).numpy()
+    np.testing.assert_allclose(oracle.qlinear(x, inp["wq"], s, b), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_qlinear_bias_only_and_linearity():
+    """With zero scales each output is sum_g bias[o, g] * (sum of x over
+    group g); doubling scales and biases doubles y; y is linear in x."""
+    import oracle
+    from seeded_inputs import bf16_bits_to_f64, qlinear_inputs
+    inp = qlinear_inputs(8, 2, 192, 5)
+    x, s, b = (bf16_bits_to_f64(inp[k]) for k in ("x", "scales", "biases"))
+    gsum = x.reshape(2, 3, 64).sum(axis=2)
+    np.testing.assert_allclose(oracle.qlinear(x, inp["wq"], np.zeros_like(s), b), gsum @ b.T, rtol=1e-13)
+    y = oracle.qlinear(x, inp["wq"], s, b)
+    np.testing.assert_allclose(oracle.qlinear(x, inp["wq"], 2 * s, 2 * b), 2 * y, rtol=1e-14)
+    np.testing.assert_allclose(oracle.qlinear(3 * x[:1] - x[1:], inp["wq"], s, b), 3 * y[:1] - y[1:],
+                               rtol=1e-12, atol=1e-12)
