@@ -530,6 +530,36 @@ def run_gpu(args, world, rank, local):
     del norm_sets
     torch.cuda.synchronize()
 
+    # 4-bit group-64 quantized mixer projections (in_proj 4480 -> 22656,
+    # out_proj 10240 -> 4480) for 1 and 4 rows of x (one cached frame of 1 or 4
+    # sessions), 4 random weight sets per shape (> L2) cycled in a graph
+    qlinear = {}
+    torch.cuda.nvtx.range_push("qlinear")
+    for name, n_in, n_out in (("in_proj", 4480, 22656), ("out_proj", 10240, 4480)):
+        wsets = []
+        for _ in range(4):
+            wsets.append((torch.randint(-2**31, 2**31 - 1, (n_out, n_in // 8), dtype=torch.int32, device=dev),
+                          (torch.rand(n_out, n_in // 64, device=dev) * 0.01).bfloat16(),
+                          (torch.rand(n_out, n_in // 64, device=dev) * -0.05).bfloat16()))
+        wbytes = n_out * n_in // 2 + 2 * n_out * (n_in // 64) * 2
+        for rows in (1, 4):
+            qx = torch.randn(rows, n_in, device=dev).bfloat16()
+            qy = torch.empty(rows, n_out, dtype=torch.bfloat16, device=dev)
+            torch.cuda.synchronize()
+
+            def q_pass():
+                for wq, sc, bi in wsets:
+                    m2.mamba2_qlinear(rows, n_in, n_out, qx, wq, sc, bi, qy, stream=stream)
+
+            q_us = _time_graph(torch, stream, q_pass, reps=20) / len(wsets)
+            qb = wbytes + rows * (n_in + n_out) * 2
+            qlinear[f"{name}_rows{rows}"] = {"in": n_in, "out": n_out, "rows": rows, "us_per_call": q_us,
+                                             "bytes_per_call": qb, "achieved_gbs": qb / (q_us * 1e-6) / 1e9,
+                                             "frac_hbm": qb / (q_us * 1e-6) / 1e9 / peaks["hbm"]}
+        del wsets
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+
     # long prefill: one layer at batch 4, T=4096 (the parity tests run all 27
     # layers of it); the whole scan and its SSD kernel alone, CUDA events
     PB, PT = 4, 4096
@@ -656,6 +686,7 @@ def run_gpu(args, world, rank, local):
             "step_frame_b1": step_frame,
             "step_64_sessions": step64,
             "gated_norm_T300": gated_norm,
+            "qlinear_4bit_g64": qlinear,
             "prefill_b4_T4096": prefill,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     mamba2_scan_chunks,
     mamba2_step_workspace_bytes,
     mamba2_gated_norm,
+    mamba2_qlinear,
     mamba2_step,
     mamba2_step_noalloc,
     mamba2_step_noalloc_max_bytes,
@@ -34,6 +35,6 @@ from ._binding import (  # noqa: F401
 
 __all__ = [
     "M2Error", "M2Dims", "BF16", "F32", "library_path", "load", "dims",
-    "mamba2_scan_workspace_bytes", "mamba2_conv_scan", "mamba2_conv_scan_varlen", "mamba2_scan_prepare_bc", "mamba2_scan_chunks", "mamba2_step_workspace_bytes", "mamba2_gated_norm",
+    "mamba2_scan_workspace_bytes", "mamba2_conv_scan", "mamba2_conv_scan_varlen", "mamba2_scan_prepare_bc", "mamba2_scan_chunks", "mamba2_step_workspace_bytes", "mamba2_gated_norm", "mamba2_qlinear",
     "mamba2_step", "mamba2_step_noalloc", "mamba2_step_noalloc_max_bytes", "mamba2_status_string", "mamba2_last_cuda_error", "mamba2_device_error",
 ]

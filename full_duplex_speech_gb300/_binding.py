@@ -60,6 +60,8 @@ def load():
         lib.mamba2_conv_scan_varlen.restype = ip
         lib.mamba2_gated_norm.argtypes = [dp, ip, vp, vp, vp, ctypes.c_float, vp, vp]
         lib.mamba2_gated_norm.restype = ip
+        lib.mamba2_qlinear.argtypes = [ip] * 5 + [vp] * 6
+        lib.mamba2_qlinear.restype = ip
         lib.mamba2_step_workspace_bytes.argtypes = [dp, ip]
         lib.mamba2_step_workspace_bytes.restype = sz
         lib.mamba2_step.argtypes = [dp, ip] + [vp] * 13 + [sz, vp]
@@ -181,6 +183,15 @@ def mamba2_gated_norm(d: M2Dims, rows, y, z, weight, eps, out, stream=None, chec
                                   _stream(stream))
     if check and rc:
         raise M2Error(rc, "mamba2_gated_norm")
+    return rc
+
+
+def mamba2_qlinear(rows, in_features, out_features, x, wq, scales, biases, y, group_size=64, bits=4,
+                   stream=None, check=True) -> int:
+    rc = load().mamba2_qlinear(int(rows), int(in_features), int(out_features), int(group_size), int(bits), _p(x),
+                               _p(wq), _p(scales), _p(biases), _p(y), _stream(stream))
+    if check and rc:
+        raise M2Error(rc, "mamba2_qlinear")
     return rc
 
 

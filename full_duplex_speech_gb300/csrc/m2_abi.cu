@@ -110,6 +110,32 @@ m2_status mamba2_device_error(void* stream, unsigned int* code) {
     return e == cudaSuccess ? M2_OK : cuda_fail(e);
 }
 
+m2_status mamba2_qlinear(int rows, int in_features, int out_features, int group_size, int bits, const void* x,
+                         const uint32_t* wq, const void* scales, const void* biases, void* y, void* stream) {
+    if (rows < 0 || in_features <= 0 || out_features <= 0 || group_size <= 0 || bits <= 0) return M2_EINVAL;
+    if (group_size != 64 || bits != 4) return M2_EUNSUPPORTED;
+    if (in_features % 64 != 0 || in_features > m2::kQlMaxIn) return M2_ESHAPE;
+    if (!x || !wq || !scales || !biases || !y) return M2_EINVAL;
+    if (!aligned16(x) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
+        (reinterpret_cast<uintptr_t>(biases) & 1u) || (reinterpret_cast<uintptr_t>(y) & 1u))
+        return M2_EALIGN;
+    int dev = 0;
+    m2_status st = current_device(&dev);
+    if (st != M2_OK) return st;
+    if (rows == 0) return M2_OK;
+    m2::QLinearArgs a;
+    a.rows = rows;
+    a.in = in_features;
+    a.out = out_features;
+    a.x = x;
+    a.wq = wq;
+    a.scales = static_cast<const uint16_t*>(scales);
+    a.biases = static_cast<const uint16_t*>(biases);
+    a.y = y;
+    cudaError_t e = m2::launch_qlinear(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M2_OK : cuda_fail(e);
+}
+
 size_t mamba2_step_workspace_bytes(const m2_dims* d, int n_sessions) {
     if (check_dims(d, false) != M2_OK || n_sessions < 0) return 0;
     return m2::step_workspace_bytes(shape_of(d), n_sessions);

@@ -5,6 +5,7 @@
 
 #include <cuda_runtime.h>
 #include <stddef.h>
+#include <stdint.h>
 
 namespace m2 {
 
@@ -59,6 +60,20 @@ struct NormArgs {
 
 // Gated RMSNorm of the mixer output (y * silu(z), grouped RMS, weight).
 cudaError_t launch_gated_norm(const NormArgs& a, cudaStream_t st);
+
+// 4-bit affine group-quantized linear layer (group 64): y = x W^T.
+constexpr int kQlMaxIn = 16384;  // input features, at most
+struct QLinearArgs {
+    int rows, in, out;
+    const void* x;            // [rows, in] bf16
+    const uint32_t* wq;       // [out, in/8]: eight 4-bit fields per word, the first input lowest
+    const uint16_t* scales;   // [out, in/64] bf16
+    const uint16_t* biases;   // [out, in/64] bf16
+    void* y;                  // [rows, out] bf16
+};
+// Rows of x the kernel takes per pass over the weights (0: `in` too large).
+int qlinear_rows_per_pass(int in);
+cudaError_t launch_qlinear(const QLinearArgs& a, cudaStream_t st);
 
 // Records a CUDA error for mamba2_last_cuda_error() on the calling thread.
 void record_cuda_error(cudaError_t e);

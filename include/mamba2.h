@@ -54,6 +54,7 @@
 #define MAMBA2_H
 
 #include <stddef.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -174,6 +175,30 @@ m2_status mamba2_scan_chunks(const m2_dims* d, const void* x, const void* B, con
  * check out. Asynchronous on `stream`. */
 m2_status mamba2_gated_norm(const m2_dims* d, int rows, const void* y, const void* z, const float* weight,
                             float eps, void* out, void* stream);
+
+/* Affine group-quantized linear layer: the Mamba layer's input and output
+ * projections as the VoiceChat 4-bit checkpoint stores them (Nemotron
+ * VoiceChat page, config.json: `quantization` with group_size 64, bits 4 for
+ * the Nemotron-H mixer projections; no bias). Weight (o, i) is the 4-bit
+ * field q at bits 4*(i%8) of the 32-bit word wq[o][i/8] (the first input in
+ * the lowest bits), dequantized per group of 64 inputs:
+ *     W[o][i] = scales[o][i/64] * q + biases[o][i/64]
+ *     y[r][o] = sum_i W[o][i] * x[r][i]
+ * accumulated in fp32 and rounded once to bf16.
+ *
+ * x: [rows, in_features] bf16, 16-byte aligned. wq: [out_features,
+ *   in_features/8] uint32, 16-byte aligned. scales, biases: [out_features,
+ *   in_features/64] bf16. y: [rows, out_features] bf16; must not alias x.
+ * Sizes: in_features a multiple of 64, at most 16384 (the Nemotron-H in_proj
+ *   has 4480 -> 22656, out_proj 10240 -> 4480); rows >= 0 (rows == 0 is a
+ *   no-op once the arguments check out). Each pass over the weights takes up
+ *   to 4 rows of x (2 for in_features above 12480), so the weight traffic
+ *   grows with rows: this form is for the few rows of a cached decode step.
+ * Errors: M2_EINVAL (NULL pointer, non-positive size), M2_EUNSUPPORTED
+ *   (group_size other than 64 or bits other than 4, or not an sm_103 GPU),
+ *   M2_ESHAPE (in_features), M2_EALIGN, M2_ECUDA. Asynchronous on `stream`. */
+m2_status mamba2_qlinear(int rows, int in_features, int out_features, int group_size, int bits, const void* x,
+                         const uint32_t* wq, const void* scales, const void* biases, void* y, void* stream);
 
 /* Bytes of device scratch that mamba2_step needs for n_sessions sessions. */
 size_t mamba2_step_workspace_bytes(const m2_dims* d, int n_sessions);

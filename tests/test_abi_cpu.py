@@ -119,3 +119,20 @@ def test_gated_norm_validation_without_gpu(m2):
     assert m2.mamba2_gated_norm(bad, 3, *p[:3], 1e-5, p[3], stream=0, check=False) == 2
     wide = m2.dims(0, 0, 512, 80, 16, 1, 4, "bf16")  # a 40960-channel group
     assert m2.mamba2_gated_norm(wide, 3, *p[:3], 1e-5, p[3], stream=0, check=False) == 4
+
+
+def test_qlinear_validation_without_gpu(m2):
+    p = _fake_ptrs(5)
+    q = lambda rows, i, o, *ptrs, g=64, b=4: m2.mamba2_qlinear(rows, i, o, *ptrs, group_size=g, bits=b,  # noqa: E731
+                                                              stream=0, check=False)
+    assert q(2, 128, 8, None, *p[1:5]) == 1            # NULL x
+    assert q(2, 128, 8, *p[:4], None) == 1             # NULL y
+    assert q(-1, 128, 8, *p) == 1                      # rows < 0
+    assert q(2, 0, 8, *p) == 1 and q(2, 128, 0, *p) == 1
+    assert q(2, 128, 8, *p, g=32) == 4                 # only group 64 ...
+    assert q(2, 128, 8, *p, b=8) == 4                  # ... and 4 bits are built
+    assert q(2, 96, 8, *p) == 2                        # in not a multiple of 64
+    assert q(2, 16384 + 64, 8, *p) == 2                # in above 16384
+    assert q(2, 128, 8, p[0] + 8, *p[1:]) == 3         # x not 16-byte aligned
+    assert q(2, 128, 8, p[0], p[1] + 4, *p[2:]) == 3   # wq not 16-byte aligned
+    assert q(2, 128, 8, *p[:2], p[2] + 1, *p[3:]) == 3  # scales odd
