@@ -76,14 +76,18 @@ __device__ __forceinline__ void bc_store_row(uint8_t* tiles, int row, int n0, in
                                              const float (&out)[8]) {
     uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
     if (live) {
-        uint32_t hb[8], lb[8];
+        // each 32-bit word: two channels rounded to bf16 (nearest even) with one
+        // paired conversion, then their residuals the same way
+        uint32_t hw[4], lw[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            hb[j] = float_to_bf16_bits(out[j]);
-            lb[j] = float_to_bf16_bits(out[j] - bf16_bits_to_float(hb[j]));
+        for (int j = 0; j < 4; ++j) {
+            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hw[j]) : "f"(out[2 * j + 1]), "f"(out[2 * j]));
+            const float r0 = out[2 * j] - __uint_as_float(hw[j] << 16);
+            const float r1 = out[2 * j + 1] - __uint_as_float(hw[j] & 0xFFFF0000u);
+            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lw[j]) : "f"(r1), "f"(r0));
         }
-        hi = make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16), hb[6] | (hb[7] << 16));
-        lo = make_uint4(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16), lb[4] | (lb[5] << 16), lb[6] | (lb[7] << 16));
+        hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
     const uint32_t off = tc::sw128_off(row, n0, kTR);
     if (which == 0) {
