@@ -59,7 +59,7 @@ WORKLOAD = ("Nemotron-H Mamba2 mixer, real shape H=128 P=80 N=128 G=8 K=4, batch
 # launch of this workload, from the ncu capture summarised in
 # profiles/scan_ssd_kernel_b1_T300.md. It describes one version of the kernel
 # source; for any other version the traffic is reported as unknown (null).
-SSD_TRAFFIC = {"bytes": 8884224, "m2_scan_cu_sha1": "752f040834e5269bae3b237542f8a6961fe0f0a3"}
+SSD_TRAFFIC = {"bytes": 8884224, "m2_scan_cu_sha1": "9e2a4ebb20f9330387da1e26c7400001fcaf45ce"}
 SCAN_BYTES_PER_TOKEN = 45312
 STATE_BYTES = 128 * 80 * 128 * 4
 TAIL_BYTES = 3 * 12288 * 2

@@ -51,9 +51,16 @@ def _tail_bits(conv_init, frame, d):
     return np.concatenate([conv_init[:, 1:], cur[:, None, :]], axis=1)
 
 
+# group sizes H/G: 4 (tiny), 16 (real), 4, 2, 1 (one head per group) and 32
+# (B and C tails read by 32 heads)
+WIDE_GROUP = Dims(H=32, P=16, N=16, G=1)
+
+
 @pytest.mark.parametrize("shape,act,S", [(TINY_SHAPE, "f32", 3), (REAL_SHAPE, "bf16", 4),
                                          (Dims(H=8, P=32, N=64, G=2), "bf16", 5),
-                                         (Dims(H=6, P=48, N=32, G=3), "f32", 2)])
+                                         (Dims(H=6, P=48, N=32, G=3), "f32", 2),
+                                         (Dims(H=4, P=16, N=16, G=4), "f32", 2),
+                                         (WIDE_GROUP, "bf16", 3)])
 def test_step_one_frame_from_random_state(m2, shape, act, S):
     d = shape
     inp = mixer_inputs(101, d, S, 1, act)
@@ -89,6 +96,26 @@ def test_step_sequence_equals_recompute(m2, act):
     y = np.stack(ys, axis=1)
     ref = oracle.mixer_scan(d, inp)
     assert y_error(y, ref["y"], act) <= Y_TOL
+    assert state_error(ssm_dev.cpu().numpy(), ref["final_ssm"]) <= STATE_TOL
+    x, B, C = (inp[k] for k in "xBC")
+    full = np.concatenate([x.reshape(S, T, -1), B.reshape(S, T, -1), C.reshape(S, T, -1)], axis=2)
+    np.testing.assert_array_equal(bits_of(conv_dev), np.ascontiguousarray(full[:, -3:]).view(np.uint8).reshape(-1))
+
+
+def test_step_sequence_equals_recompute_wide_group(m2):
+    """8 cached steps from zero state with 32 heads sharing one group's B and C
+    == the oracle's full-history scan, conv tail included."""
+    import torch
+    import oracle
+    d, act, S, T = WIDE_GROUP, "bf16", 2, 8
+    inp = mixer_inputs(108, d, S, T, act)
+    pdev = _params_dev(inp)
+    ssm_dev = torch.zeros((S, d.H, d.P, d.N), dtype=torch.float32, device="cuda")
+    conv_dev = act_empty((S, d.K - 1, d.CH), act).zero_()
+    ys = [from_dev_act(_gpu_step(m2, d, S, _frame(inp, t), pdev, ssm_dev, conv_dev, act), act)
+          for t in range(T)]
+    ref = oracle.mixer_scan(d, inp)
+    assert y_error(np.stack(ys, axis=1), ref["y"], act) <= Y_TOL
     assert state_error(ssm_dev.cpu().numpy(), ref["final_ssm"]) <= STATE_TOL
     x, B, C = (inp[k] for k in "xBC")
     full = np.concatenate([x.reshape(S, T, -1), B.reshape(S, T, -1), C.reshape(S, T, -1)], axis=2)
