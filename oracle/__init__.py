@@ -68,8 +68,10 @@ def _load():
             lib.m2o_mixer_step.argtypes = [ctypes.POINTER(_Dims), ip] + [dp] * 12 + [ip]
             lib.m2o_gated_norm.argtypes = [ip, ip, ip, dp, dp, dp, ctypes.c_double, dp]
             lib.m2o_qlinear.argtypes = [ip, ip, ip, ip, ctypes.POINTER(ctypes.c_uint32), dp, dp, dp, dp]
+            lib.m2o_attn_decode.argtypes = [ip] * 5 + [ctypes.POINTER(ctypes.c_int)] + [dp] * 5 + \
+                [ctypes.c_double, dp]
             for f in ("m2o_ssm", "m2o_conv_silu", "m2o_conv_tail", "m2o_mixer_scan", "m2o_mixer_step",
-                      "m2o_gated_norm", "m2o_qlinear"):
+                      "m2o_gated_norm", "m2o_qlinear", "m2o_attn_decode"):
                 getattr(lib, f).restype = ip
             _lib = lib
     return _lib
@@ -217,3 +219,25 @@ def qlinear(x, wq, scales, biases, group: int = 64) -> np.ndarray:
                              _ptr(_f64(biases)), _ptr(x), _ptr(y))
     _check(rc, "qlinear")
     return y
+
+
+def attn_decode(q, k_new, v_new, k_cache, v_cache, lengths, scale: float) -> np.ndarray:
+    """One cached decode position of grouped-query attention. q [S,Hq,D];
+    k_new, v_new [S,Hkv,D]; k_cache, v_cache [S,Hkv,Tmax,D] fp64 arrays,
+    UPDATED IN PLACE (the new key and value land at position lengths[s]);
+    lengths [S] ints (positions already cached). Query head h reads kv head
+    h // (Hq // Hkv) over positions 0..lengths[s]. Returns out [S,Hq,D] fp64."""
+    q = _f64(q)
+    k_new, v_new = _f64(k_new), _f64(v_new)
+    for c in (k_cache, v_cache):
+        if not (isinstance(c, np.ndarray) and c.dtype == np.float64 and c.flags.c_contiguous):
+            raise TypeError("k_cache and v_cache must be C-contiguous float64 arrays (updated in place)")
+    S, Hq, D = q.shape
+    Hkv, Tmax = k_cache.shape[1], k_cache.shape[2]
+    lens = np.ascontiguousarray(lengths, dtype=np.int32)
+    out = np.empty((S, Hq, D), dtype=np.float64)
+    rc = _load().m2o_attn_decode(S, Hq, Hkv, D, Tmax, lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                                 _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                 float(scale), _ptr(out))
+    _check(rc, "attn_decode")
+    return out

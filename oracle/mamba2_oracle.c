@@ -28,6 +28,10 @@
  *     SSM state that the VoiceChat doc ("docs/nemotron-voicechat.md", section
  *     Offline timeline, last paragraph) says must give the same result as
  *     recomputing the full history.
+ *  6. The output side of the mixer and its projections (gated RMSNorm,
+ *     4-bit affine group-quantized linear layers), and one cached decode
+ *     position of the hybrid model's grouped-query attention layers with
+ *     their KV caches (each function below cites its passage).
  *
  * Layouts (contiguous, innermost last):
  *   x [b,T,H,P]   B, C [b,T,G,N]   dt_raw [b,T,H]   y [b,T,H,P]
@@ -397,5 +401,69 @@ int m2o_qlinear(int rows, int in, int out, int group, const uint32_t* wq, const 
             for (long r = 0; r < rows; ++r) y[r * out + o] += w * x[r * in + i];
         }
     }
+    return M2O_OK;
+}
+
+/* One cached decode position of a grouped-query attention layer of the same
+ * hybrid model: the Nemotron-H attention layers (num_attention_heads 40,
+ * num_key_value_heads 8, head_dim 128, attention_bias false; the
+ * configuration lists no positional rotation for them; VoiceChat issue,
+ * section config.json / text_config, hybrid_override_pattern `*` layers),
+ * whose KV caches a session keeps across positions ("docs/nemotron-voicechat.md",
+ * section Online session, persistent-state table). For session s with
+ * len[s] positions already cached:
+ *   - each kv head's new key and value go to position len[s];
+ *   - query head h reads kv head g = h / (Hq/Hkv), over positions
+ *     t = 0 .. len[s] (the new position included):
+ *       a_t = scale * sum_d q[h][d] k[g][t][d]
+ *       w_t = exp(a_t - max_u a_u) / sum_u exp(a_u - max_u a_u)
+ *       out[h] = sum_t w_t v[g][t]
+ * q, out [S,Hq,D]; k_new, v_new [S,Hkv,D]; k_cache, v_cache [S,Hkv,Tmax,D].
+ * Positions past len[s] are neither read nor written. A len[s] outside
+ * [0, Tmax) is an error (nothing is written). */
+int m2o_attn_decode(int S, int Hq, int Hkv, int D, int Tmax, const int* len, const double* q,
+                    const double* k_new, const double* v_new, double* k_cache, double* v_cache,
+                    double scale, double* out) {
+    if (S < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Tmax <= 0 || Hq % Hkv != 0 || !len || !q || !k_new ||
+        !v_new || !k_cache || !v_cache || !out)
+        return M2O_EINVAL;
+    for (int s = 0; s < S; ++s)
+        if (len[s] < 0 || len[s] >= Tmax) return M2O_EINVAL;
+    const int R = Hq / Hkv;
+    double* a = (double*)malloc(sizeof(double) * (size_t)Tmax);
+    if (!a) return M2O_ENOMEM;
+    for (int s = 0; s < S; ++s) {
+        const int L = len[s];
+        for (int g = 0; g < Hkv; ++g) {
+            const long kv = ((long)s * Hkv + g) * Tmax;
+            for (int d = 0; d < D; ++d) {
+                k_cache[(kv + L) * D + d] = k_new[((long)s * Hkv + g) * D + d];
+                v_cache[(kv + L) * D + d] = v_new[((long)s * Hkv + g) * D + d];
+            }
+            for (int r = 0; r < R; ++r) {
+                const int h = g * R + r;
+                const double* qh = q + ((long)s * Hq + h) * D;
+                double amax = -INFINITY;
+                for (int t = 0; t <= L; ++t) {
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += qh[d] * k_cache[(kv + t) * D + d];
+                    a[t] = scale * dot;
+                    if (a[t] > amax) amax = a[t];
+                }
+                double den = 0.0;
+                for (int t = 0; t <= L; ++t) {
+                    a[t] = exp(a[t] - amax);
+                    den += a[t];
+                }
+                double* oh = out + ((long)s * Hq + h) * D;
+                for (int d = 0; d < D; ++d) {
+                    double num = 0.0;
+                    for (int t = 0; t <= L; ++t) num += a[t] * v_cache[(kv + t) * D + d];
+                    oh[d] = num / den;
+                }
+            }
+        }
+    }
+    free(a);
     return M2O_OK;
 }

@@ -236,3 +236,24 @@ def qlinear_inputs(seed: int, rows: int, in_features: int, out_features: int, gr
     biases = -7.5 * scales * rng.uniform(0.8, 1.2, size=(out_features, ng))
     return dict(x=f32_to_bf16_bits(x), wq=wq, scales=f32_to_bf16_bits(scales.astype(np.float32)),
                 biases=f32_to_bf16_bits(biases.astype(np.float32)), group=group)
+
+
+def attn_inputs(seed: int, S: int, Hq: int, Hkv: int, D: int, Tmax: int, lengths, act: str = "bf16") -> dict:
+    """One cached decode position of grouped-query attention: q [S,Hq,D],
+    k_new, v_new [S,Hkv,D] and the caches k_cache, v_cache [S,Hkv,Tmax,D],
+    all ~ N(0, 1) (the cache slots past each session's length hold values
+    too, which the position must neither read nor change); lengths [S]
+    int32. act='bf16' -> uint16 bit patterns; act='f32' -> float32."""
+    rng = np.random.default_rng([seed, 0x5EED, 7])
+    out = dict(q=rng.standard_normal((S, Hq, D), dtype=np.float32),
+               k_new=rng.standard_normal((S, Hkv, D), dtype=np.float32),
+               v_new=rng.standard_normal((S, Hkv, D), dtype=np.float32),
+               k_cache=rng.standard_normal((S, Hkv, Tmax, D), dtype=np.float32),
+               v_cache=rng.standard_normal((S, Hkv, Tmax, D), dtype=np.float32))
+    if act == "bf16":
+        out = {k: f32_to_bf16_bits(v) for k, v in out.items()}
+    elif act != "f32":
+        raise ValueError(f"act must be 'bf16' or 'f32', got {act!r}")
+    out["lengths"] = np.ascontiguousarray(lengths, dtype=np.int32)
+    out["act"] = act
+    return out

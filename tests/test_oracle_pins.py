@@ -452,3 +452,99 @@ def test_qlinear_bias_only_and_linearity():
     np.testing.assert_allclose(oracle.qlinear(x, inp["wq"], 2 * s, 2 * b), 2 * y, rtol=1e-14)
     np.testing.assert_allclose(oracle.qlinear(3 * x[:1] - x[1:], inp["wq"], s, b), 3 * y[:1] - y[1:],
                                rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- attention decode
+def _attn_case(seed, S, Hq, Hkv, D, Tmax, lengths):
+    from seeded_inputs import attn_inputs
+    inp = attn_inputs(seed, S, Hq, Hkv, D, Tmax, lengths, act="f32")
+    return {k: (v.astype(np.float64) if k not in ("lengths", "act") else v) for k, v in inp.items()}
+
+
+def test_attn_single_position_returns_the_new_value():
+    """With nothing cached the softmax has one term: every query head of a
+    group returns its kv head's new value exactly, whatever q and scale."""
+    import oracle
+    c = _attn_case(21, 2, 6, 2, 8, 4, [0, 0])
+    out = oracle.attn_decode(c["q"], c["k_new"], c["v_new"], c["k_cache"], c["v_cache"], [0, 0], 0.7)
+    np.testing.assert_array_equal(out, np.repeat(c["v_new"], 3, axis=1))
+
+
+def test_attn_equal_keys_average_the_values():
+    """Identical keys at every position give uniform weights: the output is
+    the plain mean of the values over positions 0..len."""
+    import oracle
+    c = _attn_case(22, 1, 2, 1, 8, 6, [4])
+    k = c["k_cache"]
+    k[0, 0, :4] = c["k_new"][0, 0]
+    out = oracle.attn_decode(c["q"], c["k_new"], c["v_new"], k, c["v_cache"], [4], 0.3)
+    want = np.concatenate([c["v_cache"][0, 0, :4], c["v_new"][0, 0][None]]).mean(axis=0)
+    np.testing.assert_allclose(out[0], np.stack([want, want]), rtol=1e-13, atol=1e-15)
+
+
+def test_attn_two_positions_logistic_form():
+    """Two positions: out = v0 + sigmoid(a1 - a0) (v1 - v0), a_t = scale q.k_t."""
+    import oracle
+    from scipy.special import expit
+    c = _attn_case(23, 1, 1, 1, 16, 3, [1])
+    q, k0, k1 = c["q"][0, 0], c["k_cache"][0, 0, 0], c["k_new"][0, 0]
+    v0, v1 = c["v_cache"][0, 0, 0].copy(), c["v_new"][0, 0]
+    sc = 0.25
+    a0 = sc * sum(q[i] * k0[i] for i in range(16))
+    a1 = sc * sum(q[i] * k1[i] for i in range(16))
+    out = oracle.attn_decode(c["q"], c["k_new"], c["v_new"], c["k_cache"], c["v_cache"], [1], sc)
+    np.testing.assert_allclose(out[0, 0], v0 + expit(a1 - a0) * (v1 - v0), rtol=1e-12, atol=1e-14)
+
+
+def test_attn_query_heads_read_contiguous_kv_groups():
+    """Hq = 6 query heads over Hkv = 2 kv heads: heads 0-2 read kv head 0 and
+    heads 3-5 kv head 1 (values constant per kv head give exactly that)."""
+    import oracle
+    c = _attn_case(24, 1, 6, 2, 8, 5, [3])
+    for g in range(2):
+        c["v_cache"][0, g] = g + 1.0
+        c["v_new"][0, g] = g + 1.0
+    out = oracle.attn_decode(c["q"], c["k_new"], c["v_new"], c["k_cache"], c["v_cache"], [3], 0.5)
+    np.testing.assert_array_equal(out[0, :, 0], [1, 1, 1, 2, 2, 2])
+
+
+def test_attn_shift_and_scale_invariances():
+    """Adding alpha q_h to every key of head h (Hq = Hkv) shifts all its
+    scores equally and leaves its output unchanged; the scale multiplies the
+    scores, so (scale, q) and (1, scale q) agree."""
+    import oracle
+    c = _attn_case(25, 2, 3, 3, 16, 9, [8, 5])
+    ref = oracle.attn_decode(c["q"], c["k_new"], c["v_new"], c["k_cache"].copy(), c["v_cache"].copy(),
+                             c["lengths"], 0.4)
+    shifted_k = c["k_cache"] + 0.7 * c["q"][:, :, None, :]
+    shifted_new = c["k_new"] + 0.7 * c["q"]
+    out = oracle.attn_decode(c["q"], shifted_new, c["v_new"], shifted_k, c["v_cache"].copy(), c["lengths"], 0.4)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-13)
+    out2 = oracle.attn_decode(0.4 * c["q"], c["k_new"], c["v_new"], c["k_cache"].copy(), c["v_cache"].copy(),
+                              c["lengths"], 1.0)
+    np.testing.assert_allclose(out2, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_attn_dominant_key_selects_its_value():
+    """A key at position 2 equal to 50 q (score 50 |q|^2 scale) dominates
+    every other position: the output is that position's value."""
+    import oracle
+    c = _attn_case(26, 1, 1, 1, 16, 8, [6])
+    c["k_cache"][0, 0, 2] = 50.0 * c["q"][0, 0]
+    out = oracle.attn_decode(c["q"], c["k_new"], c["v_new"], c["k_cache"], c["v_cache"], [6], 1.0)
+    np.testing.assert_allclose(out[0, 0], c["v_cache"][0, 0, 2], rtol=1e-12, atol=1e-14)
+
+
+def test_attn_appends_and_touches_nothing_else():
+    """Position len[s] receives the new key and value; every other slot keeps
+    its bits; a length outside [0, Tmax) is refused."""
+    import oracle
+    c = _attn_case(27, 3, 4, 2, 8, 6, [0, 2, 5])
+    k0, v0 = c["k_cache"].copy(), c["v_cache"].copy()
+    oracle.attn_decode(c["q"], c["k_new"], c["v_new"], c["k_cache"], c["v_cache"], c["lengths"], 0.35)
+    for s, L in enumerate(c["lengths"]):
+        k0[s, :, L], v0[s, :, L] = c["k_new"][s], c["v_new"][s]
+    np.testing.assert_array_equal(c["k_cache"], k0)
+    np.testing.assert_array_equal(c["v_cache"], v0)
+    with pytest.raises(RuntimeError):
+        oracle.attn_decode(c["q"], c["k_new"], c["v_new"], c["k_cache"], c["v_cache"], [0, 2, 6], 0.35)
