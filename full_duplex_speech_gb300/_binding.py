@@ -62,6 +62,10 @@ def load():
         lib.mamba2_gated_norm.restype = ip
         lib.mamba2_qlinear.argtypes = [ip] * 5 + [vp] * 6
         lib.mamba2_qlinear.restype = ip
+        lib.mamba2_attn_decode.argtypes = [ip] * 6 + [vp] * 6 + [ctypes.c_float, vp, vp, sz, vp]
+        lib.mamba2_attn_decode.restype = ip
+        lib.mamba2_attn_decode_workspace_bytes.argtypes = [ip] * 6
+        lib.mamba2_attn_decode_workspace_bytes.restype = sz
         lib.mamba2_step_workspace_bytes.argtypes = [dp, ip]
         lib.mamba2_step_workspace_bytes.restype = sz
         lib.mamba2_step.argtypes = [dp, ip] + [vp] * 13 + [sz, vp]
@@ -192,6 +196,35 @@ def mamba2_qlinear(rows, in_features, out_features, x, wq, scales, biases, y, gr
                                _p(wq), _p(scales), _p(biases), _p(y), _stream(stream))
     if check and rc:
         raise M2Error(rc, "mamba2_qlinear")
+    return rc
+
+
+def _act_code(act) -> int:
+    if act in ("bf16", 0):
+        return 0
+    if act in ("f32", 1):
+        return 1
+    raise ValueError(f"act must be 'bf16' or 'f32', got {act!r}")
+
+
+def mamba2_attn_decode_workspace_bytes(n_sessions, n_heads, n_kv_heads, head_dim, max_len, act="bf16") -> int:
+    return load().mamba2_attn_decode_workspace_bytes(int(n_sessions), int(n_heads), int(n_kv_heads), int(head_dim),
+                                                     int(max_len), _act_code(act))
+
+
+def mamba2_attn_decode(n_sessions, n_heads, n_kv_heads, head_dim, max_len, act, lengths, q, k_new, v_new, k_cache,
+                       v_cache, scale, out, workspace, workspace_bytes=None, stream=None, check=True) -> int:
+    """One cached decode position of grouped-query attention with the KV-cache
+    append (see mamba2_attn_decode in include/mamba2.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
+    rc = load().mamba2_attn_decode(int(n_sessions), int(n_heads), int(n_kv_heads), int(head_dim), int(max_len),
+                                   _act_code(act), _p(lengths), _p(q), _p(k_new), _p(v_new), _p(k_cache),
+                                   _p(v_cache), float(scale), _p(out), _p(workspace), int(workspace_bytes),
+                                   _stream(stream))
+    if check and rc:
+        raise M2Error(rc, "mamba2_attn_decode")
     return rc
 
 

@@ -141,6 +141,64 @@ size_t mamba2_step_workspace_bytes(const m2_dims* d, int n_sessions) {
     return m2::step_workspace_bytes(shape_of(d), n_sessions);
 }
 
+namespace {
+m2_status attn_sizes(int n_sessions, int n_heads, int n_kv_heads, int head_dim, int max_len, m2_dtype act) {
+    if (n_sessions < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || max_len <= 0) return M2_EINVAL;
+    if (act != M2_BF16 && act != M2_F32) return M2_EINVAL;
+    if (head_dim != m2::kAttnD || n_heads % n_kv_heads != 0 || n_heads / n_kv_heads > m2::kAttnMaxR)
+        return M2_ESHAPE;
+    if (n_kv_heads > 65535 || n_sessions > 65535) return M2_ESHAPE;
+    return M2_OK;
+}
+}  // namespace
+
+size_t mamba2_attn_decode_workspace_bytes(int n_sessions, int n_heads, int n_kv_heads, int head_dim, int max_len,
+                                          m2_dtype act) {
+    if (attn_sizes(n_sessions, n_heads, n_kv_heads, head_dim, max_len, act) != M2_OK) return 0;
+    return m2::attn_workspace_bytes(n_sessions, n_heads, n_kv_heads, max_len, act == M2_BF16);
+}
+
+m2_status mamba2_attn_decode(int n_sessions, int n_heads, int n_kv_heads, int head_dim, int max_len, m2_dtype act,
+                             const int32_t* lengths, const void* q, const void* k_new, const void* v_new,
+                             void* k_cache, void* v_cache, float scale, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    m2_status st = attn_sizes(n_sessions, n_heads, n_kv_heads, head_dim, max_len, act);
+    if (st != M2_OK) return st;
+    if (!isfinite(scale)) return M2_EINVAL;
+    const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, out};
+    if (!lengths) return M2_EINVAL;
+    for (const void* p : ptrs)
+        if (!p) return M2_EINVAL;
+    if (reinterpret_cast<uintptr_t>(lengths) & 3u) return M2_EALIGN;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return M2_EALIGN;
+    const size_t need = m2::attn_workspace_bytes(n_sessions, n_heads, n_kv_heads, max_len, act == M2_BF16);
+    if (need && (!workspace || workspace_bytes < need)) return M2_EWORKSPACE;
+    if (workspace && !aligned16(workspace)) return M2_EALIGN;
+    int dev = 0;
+    st = current_device(&dev);
+    if (st != M2_OK) return st;
+    if (n_sessions == 0) return M2_OK;
+    m2::AttnArgs a;
+    a.S = n_sessions;
+    a.Hq = n_heads;
+    a.Hkv = n_kv_heads;
+    a.Tmax = max_len;
+    a.bf16 = act == M2_BF16;
+    a.lens = lengths;
+    a.q = q;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.scale = scale;
+    a.out = out;
+    a.ws = static_cast<float*>(workspace);
+    a.err = g_dev_error_ptr[dev];
+    cudaError_t e = m2::launch_attn_decode(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M2_OK : cuda_fail(e);
+}
+
 m2_status mamba2_gated_norm(const m2_dims* d, int rows, const void* y, const void* z, const float* weight,
                             float eps, void* out, void* stream) {
     m2_status st = check_dims(d, false);

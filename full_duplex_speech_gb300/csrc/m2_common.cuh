@@ -170,12 +170,14 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Codes written to the device error word when a bounded wait runs out.
+// Codes written to the device error word: a bounded wait that ran out, or an
+// input that only the device sees and that the kernel refused.
 enum : unsigned int {
     ERR_NONE = 0,
     ERR_MBAR_TIMEOUT_LOAD = 0x101,
     ERR_MBAR_TIMEOUT_MMA = 0x102,
     ERR_TMEM_ALLOC = 0x103,
+    ERR_ATTN_LENGTH = 0x104,  // a cached length outside [0, max_len)
 };
 
 }  // namespace m2

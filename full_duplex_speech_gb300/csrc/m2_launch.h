@@ -75,6 +75,23 @@ struct QLinearArgs {
 int qlinear_rows_per_pass(int in);
 cudaError_t launch_qlinear(const QLinearArgs& a, cudaStream_t st);
 
+// One cached decode position of grouped-query attention with KV-cache append.
+constexpr int kAttnD = 128;     // head_dim
+constexpr int kAttnMaxR = 8;    // query heads per kv head, at most
+struct AttnArgs {
+    int S, Hq, Hkv, Tmax;
+    bool bf16;                  // activation dtype: true = bf16, false = fp32
+    const int* lens;            // [S] positions already cached (device)
+    const void *q, *k_new, *v_new;
+    void *k_cache, *v_cache;    // [S, Hkv, Tmax, D], updated at position lens[s]
+    float scale;                // softmax scale of q.k
+    void* out;                  // [S, Hq, D]
+    float* ws;                  // per-chunk partial results
+    unsigned int* err;          // device error word
+};
+size_t attn_workspace_bytes(int S, int Hq, int Hkv, int Tmax, bool bf16);
+cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st);
+
 // Records a CUDA error for mamba2_last_cuda_error() on the calling thread.
 void record_cuda_error(cudaError_t e);
 

@@ -19,6 +19,9 @@
  * cached mode give identical tokens):
  *   mamba2_conv_scan — whole history / prefill, chunked (SSD) evaluation;
  *   mamba2_step      — one frame for a batch of sessions from cached state.
+ * Around it: the gated output norm and the 4-bit projections of the Mamba
+ * layer, and the cached decode of the model's attention layers
+ * (mamba2_gated_norm, mamba2_qlinear, mamba2_attn_decode).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -199,6 +202,46 @@ m2_status mamba2_gated_norm(const m2_dims* d, int rows, const void* y, const voi
  *   M2_ESHAPE (in_features), M2_EALIGN, M2_ECUDA. Asynchronous on `stream`. */
 m2_status mamba2_qlinear(int rows, int in_features, int out_features, int group_size, int bits, const void* x,
                          const uint32_t* wq, const void* scales, const void* biases, void* y, void* stream);
+
+/* One cached decode position of the hybrid model's grouped-query attention
+ * layers, with the KV-cache append: the Nemotron-H attention layers (VoiceChat
+ * issue, section config.json / text_config: num_attention_heads 40,
+ * num_key_value_heads 8, head_dim 128, attention_bias false, and no
+ * positional rotation listed for them), whose KV caches are part of the state
+ * a session keeps ("docs/nemotron-voicechat.md", section Online session).
+ * For each session s, with lengths[s] = L positions already cached:
+ *     k_cache[s][g][L] = k_new[s][g],  v_cache[s][g][L] = v_new[s][g]
+ *     a_t   = scale * q[s][h] . k_cache[s][g][t]      for t = 0 .. L
+ *     out[s][h] = sum_t softmax(a)_t v_cache[s][g][t]
+ * where query head h reads kv head g = h / (n_heads / n_kv_heads). Scores,
+ * softmax and sums in fp32 (exp2 of log2-scaled scores), out rounded once to
+ * the activation dtype. Only slot L of each cache changes; slots past L are
+ * neither read nor written. The caller advances lengths[] between positions
+ * (all attention layers of one position share them).
+ *
+ * q, out [S, n_heads, 128]; k_new, v_new [S, n_kv_heads, 128];
+ * k_cache, v_cache [S, n_kv_heads, max_len, 128]; all in `act` (bf16 or fp32),
+ * 16-byte aligned; lengths: int32 [S] in DEVICE memory, 4-byte aligned.
+ * out must not alias any input.
+ * Sizes: head_dim 128; n_heads a multiple of n_kv_heads, at most 8 query heads
+ *   per kv head; n_kv_heads and n_sessions at most 65535; max_len >= 1.
+ *   n_sessions == 0 is a no-op once the arguments check out.
+ * Scratch: workspace of at least mamba2_attn_decode_workspace_bytes(...):
+ *   per-chunk partial results (128 positions a chunk in bf16, 64 in fp32).
+ * Errors: M2_EINVAL (NULL pointer, non-positive size, non-finite scale),
+ *   M2_ESHAPE, M2_EALIGN, M2_EWORKSPACE, M2_EUNSUPPORTED, M2_ECUDA. A length
+ *   outside [0, max_len) is seen only on the device: that session's out is
+ *   zero, its caches are untouched, and the device error word reads 0x104
+ *   (mamba2_device_error). Two kernels, asynchronous on `stream`. */
+m2_status mamba2_attn_decode(int n_sessions, int n_heads, int n_kv_heads, int head_dim, int max_len, m2_dtype act,
+                             const int32_t* lengths, const void* q, const void* k_new, const void* v_new,
+                             void* k_cache, void* v_cache, float scale, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* Bytes of device scratch that mamba2_attn_decode needs (0 if the sizes are
+ * invalid or n_sessions is 0). */
+size_t mamba2_attn_decode_workspace_bytes(int n_sessions, int n_heads, int n_kv_heads, int head_dim, int max_len,
+                                          m2_dtype act);
 
 /* Bytes of device scratch that mamba2_step needs for n_sessions sessions. */
 size_t mamba2_step_workspace_bytes(const m2_dims* d, int n_sessions);

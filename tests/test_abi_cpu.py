@@ -136,3 +136,31 @@ def test_qlinear_validation_without_gpu(m2):
     assert q(2, 128, 8, p[0] + 8, *p[1:]) == 3         # x not 16-byte aligned
     assert q(2, 128, 8, p[0], p[1] + 4, *p[2:]) == 3   # wq not 16-byte aligned
     assert q(2, 128, 8, *p[:2], p[2] + 1, *p[3:]) == 3  # scales odd
+
+
+def test_attn_decode_validation_without_gpu(m2):
+    """Every host-side check of mamba2_attn_decode, before any device call."""
+    p = _fake_ptrs(8)
+    lens, q, kn, vn, kc, vc, out, ws = p
+    big = 1 << 30
+
+    def call(S=2, Hq=40, Hkv=8, D=128, T=100, act="bf16", scale=0.088, ptrs=None, wsb=big):
+        pt = ptrs or [lens, q, kn, vn, kc, vc]
+        return m2.mamba2_attn_decode(S, Hq, Hkv, D, T, act, *pt, scale, out, ws, workspace_bytes=wsb,
+                                     stream=0, check=False)
+
+    assert call(S=-1) == 1 and call(Hq=0) == 1 and call(Hkv=0) == 1 and call(T=0) == 1
+    assert call(D=64) == 2                      # head_dim 128 only
+    assert call(Hq=40, Hkv=6) == 2              # heads not a multiple of kv heads
+    assert call(Hq=72, Hkv=8) == 2              # more than 8 query heads per kv head
+    assert call(S=65536) == 2                   # grid limit
+    assert call(scale=float("inf")) == 1 and call(scale=float("nan")) == 1
+    assert call(ptrs=[None, q, kn, vn, kc, vc]) == 1
+    assert call(ptrs=[lens, q, kn, vn, None, vc]) == 1
+    assert call(ptrs=[lens + 2, q, kn, vn, kc, vc]) == 3    # lengths not 4-byte aligned
+    assert call(ptrs=[lens, q + 8, kn, vn, kc, vc]) == 3    # q not 16-byte aligned
+    need = m2.mamba2_attn_decode_workspace_bytes(2, 40, 8, 128, 100)
+    assert need == 2 * 8 * 1 * 5 * 130 * 4     # one chunk of 128 positions per (session, kv head)
+    assert m2.mamba2_attn_decode_workspace_bytes(2, 40, 8, 128, 100, "f32") == 2 * 8 * 2 * 5 * 130 * 4
+    assert call(wsb=need - 1) == 6
+    assert m2.mamba2_attn_decode_workspace_bytes(2, 40, 8, 64, 100) == 0
