@@ -560,6 +560,47 @@ def run_gpu(args, world, rank, local):
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
 
+    # cached decode of the attention layers (40 query heads, 8 kv heads,
+    # head_dim 128): one session with 750 and 7500 frames cached (60 s and the
+    # 600 s session limit), 64 sessions with 750; sets of KV caches cycled in a
+    # graph so that together they exceed L2. Algorithmic bytes per call: every
+    # cached key and value read once, the new ones read and written to the
+    # cache, q read and out written.
+    attn = {}
+    torch.cuda.nvtx.range_push("attn_decode")
+    AHQ, AHKV, AD = 40, 8, 128
+    for name, a_s, a_len, nsets in (("b1_len750", 1, 750, 48), ("b1_len7500", 1, 7500, 8),
+                                    ("s64_len750", 64, 750, 2)):
+        a_tmax = a_len + 1
+        ga = torch.Generator(device=dev).manual_seed(91)
+        asets = []
+        for _ in range(nsets):
+            asets.append(dict(
+                kc=torch.randn((a_s, AHKV, a_tmax, AD), generator=ga, device=dev).bfloat16(),
+                vc=torch.randn((a_s, AHKV, a_tmax, AD), generator=ga, device=dev).bfloat16(),
+                q=torch.randn((a_s, AHQ, AD), generator=ga, device=dev).bfloat16(),
+                kn=torch.randn((a_s, AHKV, AD), generator=ga, device=dev).bfloat16(),
+                vn=torch.randn((a_s, AHKV, AD), generator=ga, device=dev).bfloat16(),
+                out=torch.empty((a_s, AHQ, AD), dtype=torch.bfloat16, device=dev)))
+        a_lens = torch.full((a_s,), a_len, dtype=torch.int32, device=dev)
+        a_ws = torch.empty(m2.mamba2_attn_decode_workspace_bytes(a_s, AHQ, AHKV, AD, a_tmax), dtype=torch.uint8,
+                           device=dev)
+        torch.cuda.synchronize()
+
+        def a_pass():
+            for z in asets:
+                m2.mamba2_attn_decode(a_s, AHQ, AHKV, AD, a_tmax, "bf16", a_lens, z["q"], z["kn"], z["vn"], z["kc"],
+                                      z["vc"], AD ** -0.5, z["out"], a_ws, stream=stream)
+
+        a_us = _time_graph(torch, stream, a_pass, reps=20) / nsets
+        a_bytes = a_s * AHKV * AD * 2 * (2 * a_len + 4) + a_s * AHQ * AD * 2 * 2
+        attn[name] = {"sessions": a_s, "cached_positions": a_len, "us_per_call": a_us, "bytes_per_call": a_bytes,
+                      "achieved_gbs": a_bytes / (a_us * 1e-6) / 1e9,
+                      "frac_hbm": a_bytes / (a_us * 1e-6) / 1e9 / peaks["hbm"]}
+        del asets, a_ws
+        torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+
     # long prefill: one layer at batch 4, T=4096 (the parity tests run all 27
     # layers of it); the whole scan and its SSD kernel alone, CUDA events
     PB, PT = 4, 4096
@@ -687,6 +728,7 @@ def run_gpu(args, world, rank, local):
             "step_64_sessions": step64,
             "gated_norm_T300": gated_norm,
             "qlinear_4bit_g64": qlinear,
+            "attn_decode": attn,
             "prefill_b4_T4096": prefill,
             "e2e": e2e,
             "cpu_baseline": cpu,

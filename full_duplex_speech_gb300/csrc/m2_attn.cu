@@ -14,15 +14,18 @@
 // kv head in bf16 against 4R flops per byte.
 //
 // Two kernels, both launched with programmatic dependent launch:
-//  1. attn_split_kernel: one CTA per (chunk of kTc positions, kv head,
-//     session). Two bulk copies (the TMA engine) bring the chunk's cached keys
+//  1. attn_split_kernel: one CTA per (chunk of up to 128 positions, kv head,
+//     session; shorter chunks where there would be too few CTAs to fill the
+//     GPU). Two bulk copies (the TMA engine) bring the chunk's cached keys
 //     and values into shared memory: each is one contiguous run of rows. The
 //     chunk holding position len[s] takes the new key and value from the
 //     inputs instead, and writes them into the cache there (no other CTA
 //     reads that slot). Then scores (8 lanes per position, 16 dims a lane, the
-//     R heads' dot products reduced over the 8 lanes), the chunk's softmax
-//     statistics in the log2 domain (m = max, l = sum of 2^(a - m)) and
-//     acc = sum_t 2^(a_t - m) v_t, written as the chunk's partial result.
+//     R heads' dot products reduced over the 8 lanes, q held in fp32
+//     registers), the chunk's softmax statistics in the log2 domain (m = max,
+//     l = sum of 2^(a - m)) and acc = sum_t 2^(a_t - m) v_t (16 threads per
+//     value row, 8 dims each, all R heads at once), written as the chunk's
+//     partial result.
 //  2. attn_combine_kernel: per (kv head, session), merges the chunks:
 //     M = max_i m_i, out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.
 #include "m2_common.cuh"
@@ -36,23 +39,37 @@ namespace {
 constexpr int kAttnThreads = 128;
 constexpr int kAttnWarps = kAttnThreads / 32;
 
-// Positions per chunk: 32 KB of keys and 32 KB of values per CTA.
+// Positions per chunk: 32 KB of keys and 32 KB of values per CTA (chunks of
+// 64 positions, four CTAs an SM, measured slower for one session).
 template <typename TA>
 struct AttnTile {
     static constexpr int kTc = sizeof(TA) == 2 ? 128 : 64;
     static constexpr int kRowBytes = kAttnD * (int)sizeof(TA);
     static constexpr uint32_t kK = 0;
     static constexpr uint32_t kV = kK + kTc * kRowBytes;
-    static constexpr uint32_t kS = kV + kTc * kRowBytes;           // float [kAttnMaxR][kTc]: scores, then 2^(a-m)
-    static constexpr uint32_t kM = kS + kAttnMaxR * kTc * 4;       // float [kAttnMaxR]
+    static constexpr uint32_t kS = kV + kTc * kRowBytes;           // float [kAttnMaxR][kTc]: scores
+    static constexpr uint32_t kP = kS + kAttnMaxR * kTc * 4;       // float [kTc][kAttnMaxR]: 2^(a - m)
+    static constexpr uint32_t kM = kP + kAttnMaxR * kTc * 4;       // float [kAttnMaxR]
     static constexpr uint32_t kL = kM + kAttnMaxR * 4;             // float [kAttnMaxR]
     static constexpr uint32_t kBar = kL + kAttnMaxR * 4;           // one mbarrier
     static constexpr uint32_t kFlag = kBar + 8;                    // a wait gave up
     static constexpr uint32_t kBytes = kBar + 16;
-    static_assert(kAttnMaxR * kAttnD * 4 <= kTc * kRowBytes, "the key tile holds the half-sums of acc");
+    static_assert(8 * kAttnMaxR * kAttnD * 4 <= 2 * kTc * kRowBytes, "the K and V tiles hold the 8 groups' sums");
+    static_assert(kV == kK + kTc * kRowBytes, "the K and V tiles are adjacent");
+    static_assert(kAttnThreads == kAttnD, "one thread per dim in the final sum");
 };
 
 __host__ __device__ inline int attn_chunks(int Tmax, int tc) { return (Tmax + tc - 1) / tc; }
+
+// Positions per chunk: the most a CTA holds, halved (down to 32) while the
+// grid would have fewer than two CTAs per SM of the 152-SM GB300, so that a
+// short cache of few sessions still spreads over the GPU. A function of the
+// sizes alone: the workspace query needs no device.
+int attn_chunk_len(int S, int Hkv, int Tmax, bool bf16) {
+    int tc = bf16 ? AttnTile<bf16_t>::kTc : AttnTile<float>::kTc;
+    while (tc > 32 && (long)S * Hkv * attn_chunks(Tmax, tc) < 2 * 152) tc /= 2;
+    return tc;
+}
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -60,19 +77,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float r;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
-}
-
-// acc += q . k over two bf16 pairs held in 32-bit words: mixed-precision fmas
-// (bf16 x bf16 products are exact in fp32), no unpacking.
-__device__ __forceinline__ float dot2_bf16(uint32_t qw, uint32_t kw, float acc) {
-    asm("{\n\t.reg .b16 ql, qh, kl, kh;\n\t"
-        "mov.b32 {ql, qh}, %1;\n\t"
-        "mov.b32 {kl, kh}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, ql, kl, %0;\n\t"
-        "fma.rn.f32.bf16 %0, qh, kh, %0;\n\t}"
-        : "+f"(acc)
-        : "r"(qw), "r"(kw));
-    return acc;
 }
 
 // The 16 dims of q (or k) a lane holds: the 16-byte chunks i and i + 8 of a
@@ -91,36 +95,58 @@ struct Lane16 {
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) w[c] = *reinterpret_cast<const uint4*>(row + 16 * (i + 8 * c));
     }
-};
-
-// q . k over the lane's 16 dims
-template <typename TA>
-__device__ __forceinline__ float lane_dot(const Lane16<TA>& q, const Lane16<TA>& k) {
-    float acc = 0.f;
+    // the 16 values in fp32, in the order they were loaded
+    __device__ __forceinline__ void unpack(float (&f)[16]) const {
 #pragma unroll
-    for (int c = 0; c < Lane16<TA>::kChunks; ++c) {
-        const uint32_t* qw = &q.w[c].x;
-        const uint32_t* kw = &k.w[c].x;
+        for (int c = 0; c < kChunks; ++c) {
+            const uint32_t* u = &w[c].x;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if constexpr (sizeof(TA) == 2)
-                acc = dot2_bf16(qw[j], kw[j], acc);
-            else
-                acc = fmaf(__uint_as_float(qw[j]), __uint_as_float(kw[j]), acc);
+            for (int j = 0; j < 4; ++j) {
+                if constexpr (sizeof(TA) == 2) {
+                    f[c * 8 + 2 * j] = __uint_as_float(u[j] << 16);
+                    f[c * 8 + 2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+                } else {
+                    f[c * 4 + j] = __uint_as_float(u[j]);
+                }
+            }
         }
     }
-    return acc;
-}
+};
 
+// Dims [8 dq, 8 dq + 8) of a shared-memory row in fp32 (one 16-byte read in
+// bf16, two in fp32; 16 threads read a row's 256 or 512 bytes together).
 template <typename TA>
+struct Row8 {
+    __device__ __forceinline__ static void load(const uint8_t* row, int dq, float (&f)[8]) {
+        if constexpr (sizeof(TA) == 2) {
+            const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * dq);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[2 * j] = __uint_as_float(u[j] << 16);
+                f[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+            }
+        } else {
+            const float4 a = *reinterpret_cast<const float4*>(row + 32 * dq);
+            const float4 b = *reinterpret_cast<const float4*>(row + 32 * dq + 16);
+            f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+            f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+        }
+    }
+};
+
+// RM: the most query heads per kv head this instantiation handles (registers
+// for q and the sums are sized by it).
+template <typename TA, int RM>
 __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnArgs a) {
     using L = AttnTile<TA>;
-    constexpr int TC = L::kTc;
+    constexpr int TCM = L::kTc;  // the most positions a chunk holds
     constexpr int RB = L::kRowBytes;
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* sK = smem + L::kK;
     uint8_t* sV = smem + L::kV;
-    float* sS = reinterpret_cast<float*>(smem + L::kS);
+    float* sS = reinterpret_cast<float*>(smem + L::kS);  // [kAttnMaxR][TCM] scores
+    float* sP = reinterpret_cast<float*>(smem + L::kP);  // [TCM][kAttnMaxR] 2^(a - m)
     float* sM = reinterpret_cast<float*>(smem + L::kM);
     float* sL = reinterpret_cast<float*>(smem + L::kL);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -129,16 +155,17 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnArgs a) {
     const int chunk = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int R = a.Hq / a.Hkv;
+    const int tc = a.tc;  // positions per chunk, at most TCM
 
     pdl_wait();  // the inputs and the caches may come from the previous kernel
     pdl_trigger();
     const int len = a.lens[s];
     if (len < 0 || len >= a.Tmax) return;  // refused; the combine kernel reports it
-    const int t0 = chunk * TC;
+    const int t0 = chunk * tc;
     if (t0 > len) return;                  // past this session's positions
-    const int n = min(TC, len + 1 - t0);   // positions of this chunk
+    const int n = min(tc, len + 1 - t0);   // positions of this chunk
     const int ncached = min(n, len - t0);  // of which come from the cache
-    const bool has_new = len - t0 < TC;    // position len is in this chunk
+    const bool has_new = len - t0 < tc;    // position len is in this chunk
 
     const size_t kvrow = ((size_t)s * a.Hkv + g) * a.Tmax;  // row of position 0
     const uint8_t* kc = reinterpret_cast<const uint8_t*>(a.k_cache);
@@ -167,13 +194,17 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnArgs a) {
             *reinterpret_cast<uint4*>(dst) = v;
         }
     }
-    // this lane's 16 dims of the R query heads (lanes i = lane & 7)
+    // this lane's 16 dims of the R query heads, in fp32 (lanes i = lane & 7)
     const int i8 = lane & 7, j4 = lane >> 3;
-    Lane16<TA> q[kAttnMaxR];
+    float qf[RM][16];
 #pragma unroll
-    for (int r = 0; r < kAttnMaxR; ++r)
-        if (r < R)
-            q[r].load_global(reinterpret_cast<const uint8_t*>(a.q) + ((size_t)s * a.Hq + g * R + r) * RB, i8);
+    for (int r = 0; r < RM; ++r) {
+        if (r < R) {
+            Lane16<TA> qr;
+            qr.load_global(reinterpret_cast<const uint8_t*>(a.q) + ((size_t)s * a.Hq + g * R + r) * RB, i8);
+            qr.unpack(qf[r]);
+        }
+    }
     const float sl2 = a.scale * kLog2e;
     __syncthreads();
     if (ncached > 0 && !tc::mbar_wait(bar, 0)) {
@@ -187,45 +218,66 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnArgs a) {
         return;
     }
 
-    // scores: warp w takes positions [w TC/4, (w+1) TC/4), four at a time
-    // (8 lanes each); a2 = scale log2(e) q . k, -inf past the chunk's end
-    constexpr int PW = TC / kAttnWarps;
+    // scores a2 = scale log2(e) q . k (-inf past the chunk's end): groups of
+    // four positions (8 lanes each) dealt round-robin to the warps
 #pragma unroll 2
-    for (int it = 0; it < PW / 4; ++it) {
-        const int t = warp * PW + it * 4 + j4;
-        Lane16<TA> k;
-        if (t < n) k.load_shared(sK + (size_t)t * RB, i8);
-        float d[kAttnMaxR];
+    for (int base = 4 * warp; base < tc; base += 4 * kAttnWarps) {
+        const int t = base + j4;
+        float kf[16];
+        if (t < n) {
+            Lane16<TA> kr;
+            kr.load_shared(sK + (size_t)t * RB, i8);
+            kr.unpack(kf);
+        } else {
 #pragma unroll
-        for (int r = 0; r < kAttnMaxR; ++r) d[r] = (r < R && t < n) ? lane_dot<TA>(q[r], k) : 0.f;
+            for (int e = 0; e < 16; ++e) kf[e] = 0.f;
+        }
+        // two partial sums a head: shorter dependent chains
+        float d[RM];
+#pragma unroll
+        for (int r = 0; r < RM; ++r) {
+            d[r] = 0.f;
+            if (r < R) {
+                float d1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    d[r] = fmaf(qf[r][e], kf[e], d[r]);
+                    d1 = fmaf(qf[r][e + 1], kf[e + 1], d1);
+                }
+                d[r] += d1;
+            }
+        }
 #pragma unroll
         for (int off = 1; off < 8; off <<= 1)
 #pragma unroll
-            for (int r = 0; r < kAttnMaxR; ++r)
+            for (int r = 0; r < RM; ++r)
                 if (r < R) d[r] += __shfl_xor_sync(0xffffffffu, d[r], off);
         // lane i of the position writes head i's score
 #pragma unroll
-        for (int r = 0; r < kAttnMaxR; ++r)
-            if (r == i8 && r < R) sS[r * TC + t] = t < n ? d[r] * sl2 : -INFINITY;
+        for (int r = 0; r < RM; ++r)
+            if (r == i8 && r < R && t < tc) sS[r * TCM + t] = t < n ? d[r] * sl2 : -INFINITY;
     }
     __syncthreads();
 
-    // softmax statistics per head: warp w takes heads w and w + 4
+    // softmax statistics per head (warp w takes heads w and w + 4); the
+    // weights go out position-major for the value pass
     for (int r = warp; r < R; r += kAttnWarps) {
-        float v[TC / 32];
+        float v[TCM / 32];
         float m = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < TC / 32; ++c) {
-            v[c] = sS[r * TC + c * 32 + lane];
+        for (int c = 0; c < TCM / 32; ++c) {
+            const int t = c * 32 + lane;
+            v[c] = t < tc ? sS[r * TCM + t] : -INFINITY;
             m = fmaxf(m, v[c]);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
         float l = 0.f;
 #pragma unroll
-        for (int c = 0; c < TC / 32; ++c) {
+        for (int c = 0; c < TCM / 32; ++c) {
+            const int t = c * 32 + lane;
             const float p = ex2_approx(v[c] - m);  // 0 for -inf
-            sS[r * TC + c * 32 + lane] = p;
+            if (t < tc) sP[t * kAttnMaxR + r] = p;
             l += p;
         }
 #pragma unroll
@@ -237,86 +289,89 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnArgs a) {
     }
     __syncthreads();
 
-    // acc_r = sum_t p_r[t] v_t: thread = (dims pair dp, half of the positions)
-    const int dp = tid & 63, hf = tid >> 6;
-    float acc[kAttnMaxR][2];
+    // acc_r = sum_t p_r[t] v_t: 16 threads per position (8 dims each), the 8
+    // groups of 16 taking every 8th position
+    const int grp = tid >> 4, dq = tid & 15;
+    float acc[RM][8];
 #pragma unroll
-    for (int r = 0; r < kAttnMaxR; ++r) acc[r][0] = acc[r][1] = 0.f;
-    const int ta = hf * (TC / 2), tb = min(n, ta + TC / 2);
-#pragma unroll 4
-    for (int t = ta; t < tb; ++t) {
-        float v0, v1;
-        if constexpr (sizeof(TA) == 2) {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(sV + (size_t)t * RB + 4 * dp);
-            v0 = __uint_as_float(w << 16);
-            v1 = __uint_as_float(w & 0xFFFF0000u);
-        } else {
-            const float2 w = *reinterpret_cast<const float2*>(sV + (size_t)t * RB + 8 * dp);
-            v0 = w.x;
-            v1 = w.y;
-        }
+    for (int r = 0; r < RM; ++r)
 #pragma unroll
-        for (int r = 0; r < kAttnMaxR; ++r) {
-            if (r < R) {
-                const float p = sS[r * TC + t];
-                acc[r][0] = fmaf(p, v0, acc[r][0]);
-                acc[r][1] = fmaf(p, v1, acc[r][1]);
-            }
-        }
+        for (int e = 0; e < 8; ++e) acc[r][e] = 0.f;
+#pragma unroll 2
+    for (int t = grp; t < n; t += 8) {
+        float vf[8];
+        Row8<TA>::load(sV + (size_t)t * RB, dq, vf);
+        const float4 p0 = *reinterpret_cast<const float4*>(sP + t * kAttnMaxR);
+        const float4 p1 = *reinterpret_cast<const float4*>(sP + t * kAttnMaxR + 4);
+        const float pr[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+        for (int r = 0; r < RM; ++r)
+            if (r < R)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[r][e] = fmaf(pr[r], vf[e], acc[r][e]);
     }
-    // the second half's sums through shared memory (the key tile is free now)
-    float* sAcc = reinterpret_cast<float*>(sK);
-    if (hf == 1) {
+    // the 8 groups' sums through shared memory (over the K and V tiles, once
+    // every thread is done reading them)
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(sK);  // [8][R][kAttnD]
 #pragma unroll
-        for (int r = 0; r < kAttnMaxR; ++r)
-            if (r < R) *reinterpret_cast<float2*>(sAcc + r * kAttnD + 2 * dp) = make_float2(acc[r][0], acc[r][1]);
+    for (int r = 0; r < RM; ++r) {
+        if (r < R) {
+            float* dst = red + (grp * R + r) * kAttnD + 8 * dq;
+            *reinterpret_cast<float4*>(dst) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+        }
     }
     __syncthreads();
-    if (hf == 0) {
-        const int nch = attn_chunks(a.Tmax, TC);
-        const size_t part = ((size_t)s * a.Hkv + g) * nch + chunk;  // this chunk's partial result
-        float* wacc = a.ws + part * R * kAttnD;
+    const int nch = attn_chunks(a.Tmax, tc);
+    const size_t part = ((size_t)s * a.Hkv + g) * nch + chunk;  // this chunk's partial result
+    float* wacc = a.ws + part * R * kAttnD;
+    for (int r = 0; r < R; ++r) {
+        float sum = 0.f;
 #pragma unroll
-        for (int r = 0; r < kAttnMaxR; ++r) {
-            if (r < R) {
-                const float2 o = *reinterpret_cast<const float2*>(sAcc + r * kAttnD + 2 * dp);
-                *reinterpret_cast<float2*>(wacc + r * kAttnD + 2 * dp) = make_float2(acc[r][0] + o.x, acc[r][1] + o.y);
-            }
-        }
-        if (tid < R) {
-            float* wml = a.ws + (size_t)a.S * a.Hkv * nch * R * kAttnD + part * R * 2;
-            *reinterpret_cast<float2*>(wml + 2 * tid) = make_float2(sM[tid], sL[tid]);
-        }
+        for (int q = 0; q < 8; ++q) sum += red[(q * R + r) * kAttnD + tid];
+        wacc[r * kAttnD + tid] = sum;
+    }
+    if (tid < R) {
+        float* wml = a.ws + (size_t)a.S * a.Hkv * nch * R * kAttnD + part * R * 2;
+        *reinterpret_cast<float2*>(wml + 2 * tid) = make_float2(sM[tid], sL[tid]);
     }
 }
 
 // out_h = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i over the chunks of
-// session s; thread = (query head r of kv head g, dims pair).
+// session s; thread = (query head r of kv head g, dims pair). The 64 threads
+// of a head find M together (every 64th chunk each); the sum over chunks is
+// unrolled so that its loads are in flight together.
 template <typename TA>
-__global__ void attn_combine_kernel(AttnArgs a) {
-    constexpr int TC = AttnTile<TA>::kTc;
+__global__ void __launch_bounds__(kAttnMaxR * 64) attn_combine_kernel(AttnArgs a) {
+    __shared__ float sMax[kAttnMaxR][2];
     const int g = blockIdx.x, s = blockIdx.y;
+    const int tc = a.tc;
     const int R = a.Hq / a.Hkv;
-    const int r = threadIdx.x >> 6, dp = threadIdx.x & 63;
+    const int r = threadIdx.x >> 6, dp = threadIdx.x & 63, lane = threadIdx.x & 31;
     pdl_wait();  // the split kernel's partial results
     pdl_trigger();
     const int len = a.lens[s];
-    const size_t o = ((size_t)s * a.Hq + g * R + r) * kAttnD + 2 * dp;
+    const bool bad = len < 0 || len >= a.Tmax;  // the same for the whole block
+    const int nch = attn_chunks(a.Tmax, tc);
+    const int nc = bad ? 0 : len / tc + 1;  // chunks holding positions 0..len
+    const size_t part0 = ((size_t)s * a.Hkv + g) * nch;
+    const float* wml = a.ws + (size_t)a.S * a.Hkv * nch * R * kAttnD;
+    float m = -INFINITY;
+    for (int c = dp; c < nc; c += 64) m = fmaxf(m, wml[((part0 + c) * R + r) * 2]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) sMax[r][dp >> 5] = m;
+    __syncthreads();
     float v0 = 0.f, v1 = 0.f;
-    if (len < 0 || len >= a.Tmax) {
-        if (threadIdx.x == 0) atomicOr(a.err, ERR_ATTN_LENGTH);
-    } else {
-        const int nch = attn_chunks(a.Tmax, TC);
-        const int nc = len / TC + 1;  // chunks holding positions 0..len
-        const size_t part0 = ((size_t)s * a.Hkv + g) * nch;
-        const float* wml = a.ws + (size_t)a.S * a.Hkv * nch * R * kAttnD;
-        float M = -INFINITY;
-        for (int c = 0; c < nc; ++c) M = fmaxf(M, wml[((part0 + c) * R + r) * 2]);
+    if (!bad) {
+        const float M = fmaxf(sMax[r][0], sMax[r][1]);
         float den = 0.f;
+#pragma unroll 8
         for (int c = 0; c < nc; ++c) {
             const float2 ml = *reinterpret_cast<const float2*>(wml + ((part0 + c) * R + r) * 2);
-            const float f = ex2_approx(ml.x - M);
             const float2 acc = *reinterpret_cast<const float2*>(a.ws + ((part0 + c) * R + r) * kAttnD + 2 * dp);
+            const float f = ex2_approx(ml.x - M);
             v0 = fmaf(f, acc.x, v0);
             v1 = fmaf(f, acc.y, v1);
             den = fmaf(f, ml.y, den);
@@ -324,7 +379,10 @@ __global__ void attn_combine_kernel(AttnArgs a) {
         const float inv = 1.f / den;
         v0 *= inv;
         v1 *= inv;
+    } else if (threadIdx.x == 0) {
+        atomicOr(a.err, ERR_ATTN_LENGTH);
     }
+    const size_t o = ((size_t)s * a.Hq + g * R + r) * kAttnD + 2 * dp;
     if constexpr (sizeof(TA) == 2) {
         const uint32_t w = (uint32_t)float_to_bf16_bits(v0) | ((uint32_t)float_to_bf16_bits(v1) << 16);
         *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(a.out) + o) = w;
@@ -333,22 +391,30 @@ __global__ void attn_combine_kernel(AttnArgs a) {
     }
 }
 
-template <typename TA>
-cudaError_t launch_attn_typed(const AttnArgs& a, cudaStream_t st) {
+template <typename TA, int RM>
+cudaError_t launch_split(const AttnArgs& a, cudaStream_t st) {
     using L = AttnTile<TA>;
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(attn_split_kernel<TA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
+        e = cudaFuncSetAttribute(attn_split_kernel<TA, RM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)L::kBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    const int nch = attn_chunks(a.Tmax, L::kTc);
-    e = launch_pdl(attn_split_kernel<TA>, dim3(nch, a.Hkv, a.S), dim3(kAttnThreads), L::kBytes, st, a);
-    if (e != cudaSuccess) return e;
+    const int nch = attn_chunks(a.Tmax, a.tc);
+    return launch_pdl(attn_split_kernel<TA, RM>, dim3(nch, a.Hkv, a.S), dim3(kAttnThreads), L::kBytes, st, a);
+}
+
+template <typename TA>
+cudaError_t launch_attn_typed(const AttnArgs& a, cudaStream_t st) {
     const int R = a.Hq / a.Hkv;
+    // register sets for up to 2, 5 (the Nemotron-H layers) or 8 query heads per kv head
+    cudaError_t e = R <= 2 ? launch_split<TA, 2>(a, st) : R <= 5 ? launch_split<TA, 5>(a, st)
+                                                                 : launch_split<TA, 8>(a, st);
+    if (e != cudaSuccess) return e;
     return launch_pdl(attn_combine_kernel<TA>, dim3(a.Hkv, a.S), dim3(R * (kAttnD / 2)), 0, st, a);
 }
 
@@ -356,13 +422,15 @@ cudaError_t launch_attn_typed(const AttnArgs& a, cudaStream_t st) {
 
 size_t attn_workspace_bytes(int S, int Hq, int Hkv, int Tmax, bool bf16) {
     if (S <= 0 || Hq <= 0 || Hkv <= 0 || Tmax <= 0 || Hq % Hkv) return 0;
-    const int tc = bf16 ? AttnTile<bf16_t>::kTc : AttnTile<float>::kTc;
+    const int tc = attn_chunk_len(S, Hkv, Tmax, bf16);
     const size_t parts = (size_t)S * Hkv * attn_chunks(Tmax, tc) * (Hq / Hkv);
     return parts * (kAttnD + 2) * sizeof(float);
 }
 
-cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
-    if (a.S == 0) return cudaSuccess;
+cudaError_t launch_attn_decode(const AttnArgs& a0, cudaStream_t st) {
+    if (a0.S == 0) return cudaSuccess;
+    AttnArgs a = a0;
+    a.tc = attn_chunk_len(a.S, a.Hkv, a.Tmax, a.bf16);
     return a.bf16 ? launch_attn_typed<bf16_t>(a, st) : launch_attn_typed<float>(a, st);
 }
 

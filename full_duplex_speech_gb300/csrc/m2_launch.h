@@ -88,6 +88,7 @@ struct AttnArgs {
     void* out;                  // [S, Hq, D]
     float* ws;                  // per-chunk partial results
     unsigned int* err;          // device error word
+    int tc;                     // positions per chunk (set by the launcher)
 };
 size_t attn_workspace_bytes(int S, int Hq, int Hkv, int Tmax, bool bf16);
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st);

@@ -227,7 +227,8 @@ m2_status mamba2_qlinear(int rows, int in_features, int out_features, int group_
  *   per kv head; n_kv_heads and n_sessions at most 65535; max_len >= 1.
  *   n_sessions == 0 is a no-op once the arguments check out.
  * Scratch: workspace of at least mamba2_attn_decode_workspace_bytes(...):
- *   per-chunk partial results (128 positions a chunk in bf16, 64 in fp32).
+ *   per-chunk partial results (chunks of up to 128 positions in bf16, 64 in
+ *   fp32; shorter where few sessions and kv heads would leave the GPU idle).
  * Errors: M2_EINVAL (NULL pointer, non-positive size, non-finite scale),
  *   M2_ESHAPE, M2_EALIGN, M2_EWORKSPACE, M2_EUNSUPPORTED, M2_ECUDA. A length
  *   outside [0, max_len) is seen only on the device: that session's out is

@@ -77,8 +77,8 @@ def _expected_cache_bits(cache, new, lengths):
 
 
 @pytest.mark.parametrize("act,lengths", [
-    ("bf16", [0, 1, 127, 128, 129, 255, 256, 299]),  # chunk edges of 128 positions, ragged tails
-    ("f32", [0, 63, 64, 65, 200, 299]),               # chunks of 64 in fp32
+    ("bf16", [0, 1, 63, 64, 65, 127, 128, 299]),  # chunk edges (64 positions here), ragged tails
+    ("f32", [0, 31, 32, 33, 200, 299]),           # chunks of 32 here in fp32
 ])
 def test_attn_decode_chunk_edges_real_heads(m2, act, lengths):
     S, Tmax = len(lengths), 300
