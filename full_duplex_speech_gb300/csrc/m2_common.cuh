@@ -137,11 +137,8 @@ __device__ __forceinline__ float softplus_f32(float z) {
     return z > 0.f ? z + log1pf(expf(-z)) : log1pf(expf(z));
 }
 
-// SiLU(u) = u * sigmoid(u) = u / (1 + e^-u); for u -> -inf it tends to -0.
-__device__ __forceinline__ float silu_f32(float u) { return u / (1.f + expf(-u)); }
-
-// The same with the fast exponential and division intrinsics (relative error
-// ~1e-7 here). Where the divisor is huge (u below about -87) the fast
+// SiLU(u) = u * sigmoid(u) = u / (1 + e^-u), with the fast exponential and
+// division intrinsics (relative error ~1e-7 here). Where the divisor is huge (u below about -87) the fast
 // division returns 0 (its reciprocal of a value above 2^126, or of +inf, is
 // 0), where the exact result is below 1e-36 in magnitude.
 __device__ __forceinline__ float silu_fast(float u) { return __fdividef(u, 1.f + __expf(-u)); }
