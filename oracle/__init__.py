@@ -172,6 +172,35 @@ def mixer_scan(d: Dims, inp: dict, init_ssm=None, init_conv=None, chunk: int = 0
     return dict(y=y, final_ssm=fs, final_conv=fc)
 
 
+def mixer_scan_magnitude(d: Dims, inp: dict, init_ssm=None, init_conv=None, heads=None, nthreads: int = 0):
+    """Magnitude of each y element's state-space terms: the recurrence run on
+    the absolute values of the post-conv x~, B~, C~ and of the initial state,
+    with D = 0:
+        hbar_t = exp(dt A) hbar_{t-1} + dt |x~_t| (outer) |B~_t|,   ybar_t = |C~_t| . hbar_t
+    so ybar_t = sum over every term of y_t's state-space part of its absolute
+    value. A contraction whose operands are each rounded with relative error
+    at most u (bf16: u = 2^-8) is off from the exact value by at most about
+    (number of roundings per term) * u * ybar_t: the elementwise forward error
+    bound of the bf16-operand chunked scan. Composed of this module's own conv,
+    softplus and recurrence. Returns ybar [b,T,H,P] (heads outside `heads`
+    stay zero)."""
+    act = inp["act"]
+    x, B, C, dtr = (as_f64(inp[k], act) for k in ("x", "B", "C", "dt_raw"))
+    b, T = x.shape[0], x.shape[1]
+    ic = None if init_conv is None else as_f64(init_conv, act)
+    u = conv_silu(d, x, B, C, inp["conv_w"], inp["conv_b"], init_conv=ic, nthreads=nthreads)
+    HP, GN = d.H * d.P, d.G * d.N
+    xt = np.abs(u[:, :, :HP]).reshape(b, T, d.H, d.P)
+    Bt = np.abs(u[:, :, HP:HP + GN]).reshape(b, T, d.G, d.N)
+    Ct = np.abs(u[:, :, HP + GN:]).reshape(b, T, d.G, d.N)
+    sp = np.vectorize(softplus, otypes=[np.float64])
+    dt = sp(dtr + _f64(inp["dt_bias"])[None, None, :]) if dtr.size else np.zeros_like(dtr)
+    A = -np.exp(_f64(inp["A_log"]))
+    h0 = None if init_ssm is None else np.abs(_f64(init_ssm))
+    ybar, _ = ssm(d, xt, Bt, Ct, dt, A, np.zeros(d.H), h0=h0, heads=heads, nthreads=nthreads)
+    return ybar
+
+
 def mixer_step(d: Dims, frame: dict, params: dict, ssm_state, conv_state, nthreads: int = 0):
     """One cached frame for S sessions. frame holds x [S,H,P], B/C [S,G,N],
     dt_raw [S,H] (bf16 bits or fp32, with 'act'); ssm_state [S,H,P,N] and

@@ -4,19 +4,19 @@ through the C ABI: the Nemotron-H attention layers (40 query heads, 8 kv
 heads, head_dim 128; VoiceChat issue, section config.json / text_config) and
 their KV caches ("docs/nemotron-voicechat.md", section Online session).
 
-Tolerances: a bf16 output is held to the library's bar for bf16 results
-(normwise 2e-3 against the oracle rounded to bf16) and, tighter, to at most
-0.1% of its elements more than one bf16 ulp from the rounded oracle; an fp32
-output to normwise 1e-5 (fp32 dot products of 128 terms and sums over at most
-a few thousand positions: about 1e-6). The caches must change in exactly
+Tolerances: a bf16 output is held to the library's gates for bf16 results
+(normwise 2e-3 against the oracle rounded to bf16, at most 0.1% of its
+elements more than one bf16 ulp from it, none beyond 4 ulp + 1e-3 max|ref|);
+an fp32 output to normwise and max-normwise 1e-5 (fp32 dot products of 128
+terms and sums over at most a few thousand positions: about 1e-6). The caches must change in exactly
 one slot per session and kv head, to the new key's and value's bits."""
 import math
 
 import numpy as np
 import pytest
 
-from m2_testlib import Y_TOL, act_empty, bits_of, from_dev_act, to_dev, y_error
-from seeded_inputs import attn_inputs, bf16_bits_to_f64, f64_to_bf16_bits
+from m2_testlib import act_empty, bits_of, check_y, from_dev_act, to_dev
+from seeded_inputs import attn_inputs, bf16_bits_to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -61,12 +61,9 @@ def _oracle(inp, scale):
 
 def _check(out, ref, act):
     if act == "bf16":
-        assert y_error(out, ref, act) <= Y_TOL
-        rref = bf16_bits_to_f64(f64_to_bf16_bits(ref))
-        ulp = np.maximum(np.abs(rref), 2.0 ** -126) * 2.0 ** -7
-        assert float(np.mean(np.abs(out - rref) > 1.0001 * ulp)) <= 1e-3
+        check_y(out, ref, act)
     else:
-        assert y_error(out, ref, act) <= F32_TOL
+        check_y(out, ref, act, l2_tol=F32_TOL, f32_maxnorm=F32_TOL)
 
 
 def _expected_cache_bits(cache, new, lengths):

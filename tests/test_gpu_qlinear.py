@@ -8,7 +8,7 @@ passes, the smallest and largest input widths, and the real projection shapes
 import numpy as np
 import pytest
 
-from m2_testlib import Y_TOL, from_dev_act, to_dev, y_error
+from m2_testlib import check_y, from_dev_act, to_dev
 from seeded_inputs import bf16_bits_to_f64, qlinear_inputs
 
 pytestmark = pytest.mark.gpu
@@ -46,7 +46,7 @@ def oracle_qlinear(inp):
 def test_qlinear_shapes(m2, rows, n_in, n_out):
     inp = qlinear_inputs(rows * 1000 + n_in + n_out, rows, n_in, n_out)
     y = gpu_qlinear(m2, inp, rows, n_in, n_out)
-    assert y_error(from_dev_act(y, "bf16"), oracle_qlinear(inp), "bf16") <= Y_TOL
+    check_y(from_dev_act(y, "bf16"), oracle_qlinear(inp), "bf16")
 
 
 @pytest.mark.parametrize("rows,n_in,n_out", [(1, 4480, 22656), (4, 4480, 22656), (1, 10240, 4480),
@@ -54,7 +54,7 @@ def test_qlinear_shapes(m2, rows, n_in, n_out):
 def test_qlinear_nemotron_projections(m2, rows, n_in, n_out):
     inp = qlinear_inputs(77 + rows, rows, n_in, n_out)
     y = gpu_qlinear(m2, inp, rows, n_in, n_out)
-    assert y_error(from_dev_act(y, "bf16"), oracle_qlinear(inp), "bf16") <= Y_TOL
+    check_y(from_dev_act(y, "bf16"), oracle_qlinear(inp), "bf16")
 
 
 def test_qlinear_worked_example(m2):

@@ -6,8 +6,7 @@ timeline)."""
 import numpy as np
 import pytest
 
-from m2_testlib import (STATE_TOL, Y_TOL, act_empty, bits_of, from_dev_act, state_error, to_dev,
-                        y_error)
+from m2_testlib import act_empty, bits_of, check_state, check_y, from_dev_act, to_dev
 from seeded_inputs import (REAL_SHAPE, TINY_SHAPE, Dims, as_f64, conv_state_inputs, mixer_inputs,
                            ssm_state_inputs)
 
@@ -74,8 +73,8 @@ def test_step_one_frame_from_random_state(m2, shape, act, S):
     import oracle
     y_ref = oracle.mixer_step(d, _frame(inp, 0), inp, ssm_ref, conv_ref)
 
-    assert y_error(from_dev_act(y, act), y_ref, act) <= Y_TOL
-    assert state_error(ssm_dev.cpu().numpy(), ssm_ref) <= STATE_TOL
+    check_y(from_dev_act(y, act), y_ref, act)
+    check_state(ssm_dev.cpu().numpy(), ssm_ref)
     exp_tail = _tail_bits(conv0, _frame(inp, 0), d)
     np.testing.assert_array_equal(bits_of(conv_dev), np.ascontiguousarray(exp_tail).view(np.uint8).reshape(-1))
 
@@ -95,8 +94,8 @@ def test_step_sequence_equals_recompute(m2, act):
           for t in range(T)]
     y = np.stack(ys, axis=1)
     ref = oracle.mixer_scan(d, inp)
-    assert y_error(y, ref["y"], act) <= Y_TOL
-    assert state_error(ssm_dev.cpu().numpy(), ref["final_ssm"]) <= STATE_TOL
+    check_y(y, ref["y"], act)
+    check_state(ssm_dev.cpu().numpy(), ref["final_ssm"])
     x, B, C = (inp[k] for k in "xBC")
     full = np.concatenate([x.reshape(S, T, -1), B.reshape(S, T, -1), C.reshape(S, T, -1)], axis=2)
     np.testing.assert_array_equal(bits_of(conv_dev), np.ascontiguousarray(full[:, -3:]).view(np.uint8).reshape(-1))
@@ -115,8 +114,8 @@ def test_step_sequence_equals_recompute_wide_group(m2):
     ys = [from_dev_act(_gpu_step(m2, d, S, _frame(inp, t), pdev, ssm_dev, conv_dev, act), act)
           for t in range(T)]
     ref = oracle.mixer_scan(d, inp)
-    assert y_error(np.stack(ys, axis=1), ref["y"], act) <= Y_TOL
-    assert state_error(ssm_dev.cpu().numpy(), ref["final_ssm"]) <= STATE_TOL
+    check_y(np.stack(ys, axis=1), ref["y"], act)
+    check_state(ssm_dev.cpu().numpy(), ref["final_ssm"])
     x, B, C = (inp[k] for k in "xBC")
     full = np.concatenate([x.reshape(S, T, -1), B.reshape(S, T, -1), C.reshape(S, T, -1)], axis=2)
     np.testing.assert_array_equal(bits_of(conv_dev), np.ascontiguousarray(full[:, -3:]).view(np.uint8).reshape(-1))
@@ -134,8 +133,8 @@ def test_step_many_sessions_real_shape(m2):
     ssm_ref = ssm0.astype(np.float64).copy()
     conv_ref = as_f64(conv0, act).copy()
     y_ref = oracle.mixer_step(d, _frame(inp, 0), inp, ssm_ref, conv_ref, nthreads=0)
-    assert y_error(from_dev_act(y, act), y_ref, act) <= Y_TOL
-    assert state_error(ssm_dev.cpu().numpy(), ssm_ref) <= STATE_TOL
+    check_y(from_dev_act(y, act), y_ref, act)
+    check_state(ssm_dev.cpu().numpy(), ssm_ref)
 
 
 def test_step_zero_sessions_is_a_noop(m2):
@@ -178,8 +177,8 @@ def test_step_session_counts_real_shape(m2, S):
     ssm_ref = ssm0.astype(np.float64).copy()
     conv_ref = as_f64(conv0, act).copy()
     y_ref = oracle.mixer_step(d, _frame(inp, 0), inp, ssm_ref, conv_ref, nthreads=0)
-    assert y_error(from_dev_act(y, act), y_ref, act) <= Y_TOL
-    assert state_error(ssm_dev.cpu().numpy(), ssm_ref) <= STATE_TOL
+    check_y(from_dev_act(y, act), y_ref, act)
+    check_state(ssm_dev.cpu().numpy(), ssm_ref)
     exp_tail = _tail_bits(conv0, _frame(inp, 0), d)
     np.testing.assert_array_equal(bits_of(conv_dev), np.ascontiguousarray(exp_tail).view(np.uint8).reshape(-1))
 
@@ -200,5 +199,5 @@ def test_step_saturated_silu_channels(m2):
     import oracle
     y_ref = oracle.mixer_step(d, _frame(inp, 0), inp, ssm_ref, conv_ref)
     assert np.isfinite(from_dev_act(y, act)).all()
-    assert y_error(from_dev_act(y, act), y_ref, act) <= Y_TOL
-    assert state_error(ssm_dev.cpu().numpy(), ssm_ref) <= STATE_TOL
+    check_y(from_dev_act(y, act), y_ref, act)
+    check_state(ssm_dev.cpu().numpy(), ssm_ref)

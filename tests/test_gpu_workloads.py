@@ -8,13 +8,15 @@ configurations the benchmark uses, against the fp64 oracle:
   section Offline timeline: cached stepping and full-history recompute agree);
 * 64 sessions, each carried to a random length of 50-500 frames by a GPU scan
   (checked against the oracle), then one cached step for all 64 at once;
-* long prefill: batch 4, T=4096, all 27 layers back to back, sampled heads of
-  every layer checked (y and final state) and every layer's conv tail.
+* long prefill: batch 4, T=4096, all 27 layers back to back: every layer's
+  conv tail bit for bit and its whole final state against a recompute of the
+  same layer with chunks of 64; on layers 0, 13 and 26 two heads' y and final
+  state against the oracle.
 """
 import numpy as np
 import pytest
 
-from m2_testlib import STATE_TOL, Y_TOL, act_empty, bits_of, from_dev_act, state_error, to_dev, y_error
+from m2_testlib import Y_TOL, act_empty, bits_of, check_scan_y, check_state, check_y, from_dev_act, to_dev
 from seeded_inputs import MAMBA_LAYERS, REAL_SHAPE, device_mixer_inputs, mixer_inputs
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -65,19 +67,20 @@ def test_cached_decode_27_layers_750_frames(m2):
                 states[t + 1] = ssm.cpu().numpy().copy()
         torch.cuda.synchronize()
         ref = oracle.mixer_scan(d, inp)
+        ybar = oracle.mixer_scan_magnitude(d, inp)  # row n-1 is also that of a scan over n frames
         for n in checks:
             # the step against the oracle's recompute of the first n frames
-            assert y_error(ys[n], ref["y"][:, n - 1], "bf16") <= Y_TOL, (layer, n)
+            check_y(ys[n], ref["y"][:, n - 1], "bf16", tag=f"step L{layer} n{n}")
             if n == T:
-                assert state_error(states[n], ref["final_ssm"]) <= STATE_TOL, (layer, n)
+                check_state(states[n], ref["final_ssm"], tag=f"step state L{layer}")
             # the step against the GPU's own chunked recompute of the first n frames
             sub = {k: v[:, :n].contiguous() if k in ("x", "B", "C", "dt_raw") else v for k, v in dv.items()}
             ysc, fs, _ = _scan(m2, d, sub, 1, n)
             torch.cuda.synchronize()
             ylast = from_dev_act(ysc[:, n - 1], "bf16")
+            check_scan_y(ylast, ref["y"][:, n - 1], ybar[:, n - 1], "bf16", tag=f"scan L{layer} n{n}")
             assert np.linalg.norm(ys[n] - ylast) / np.linalg.norm(ylast) <= Y_TOL, (layer, n)
-            s_sc = fs.cpu().numpy().astype(np.float64)
-            assert state_error(states[n], s_sc) <= STATE_TOL, (layer, n)
+            check_state(states[n], fs.cpu().numpy().astype(np.float64), tag=f"step vs scan state L{layer} n{n}")
         np.testing.assert_array_equal(
             bits_of(conv), np.ascontiguousarray(np.concatenate(
                 [inp["x"].reshape(1, T, -1), inp["B"].reshape(1, T, -1), inp["C"].reshape(1, T, -1)],
@@ -109,10 +112,11 @@ def test_64_sessions_from_scanned_states(m2):
         r = oracle.mixer_scan(d, seq)
         ref_ssm[s], ref_conv[s] = r["final_ssm"][0], r["final_conv"][0]
         if s % 16 == 0:  # the prefix scans themselves, on a sample of sessions
-            assert y_error(from_dev_act(y, "bf16"), r["y"], "bf16") <= Y_TOL
-            assert state_error(fs.cpu().numpy(), r["final_ssm"]) <= STATE_TOL
+            check_scan_y(from_dev_act(y, "bf16"), r["y"], oracle.mixer_scan_magnitude(d, seq), "bf16",
+                         tag=f"prefix scan {s}")
+            check_state(fs.cpu().numpy(), r["final_ssm"], tag=f"prefix state {s}")
     torch.cuda.synchronize()
-    assert state_error(ssm.cpu().numpy(), ref_ssm) <= STATE_TOL
+    check_state(ssm.cpu().numpy(), ref_ssm, tag="scanned states")
     fr = {k: np.concatenate([f[k] for f in frames], axis=0) for k in ("x", "B", "C", "dt_raw")}
     fd = {k: to_dev(v) for k, v in fr.items()}
     dims = m2.dims(0, 0, d.H, d.P, d.N, d.G, d.K, "bf16")
@@ -124,8 +128,8 @@ def test_64_sessions_from_scanned_states(m2):
     # the oracle's step continues from the oracle's own scanned states
     fr["act"] = "bf16"
     y_ref = oracle.mixer_step(d, fr, base, ref_ssm, ref_conv)
-    assert y_error(from_dev_act(y1, "bf16"), y_ref, "bf16") <= Y_TOL
-    assert state_error(ssm.cpu().numpy(), ref_ssm) <= STATE_TOL
+    check_y(from_dev_act(y1, "bf16"), y_ref, "bf16", tag="64-session step")
+    check_state(ssm.cpu().numpy(), ref_ssm, tag="64-session state")
 
 
 def test_long_prefill_27_layers_b4_T4096(m2):
@@ -142,6 +146,12 @@ def test_long_prefill_27_layers_b4_T4096(m2):
         tail = torch.cat([dv["x"][:, -3:].reshape(b, 3, -1), dv["B"][:, -3:].reshape(b, 3, -1),
                           dv["C"][:, -3:].reshape(b, 3, -1)], dim=2)
         assert torch.equal(fc.view(torch.int16), tail.contiguous().view(torch.int16))
+        # every head's final state against the GPU's own recompute with chunks
+        # of 64 (the chunked form does not depend on the chunk length)
+        _, fs64, _ = _scan(m2, d, dv, b, T, chunk=64)
+        torch.cuda.synchronize()
+        check_state(fs.cpu().numpy(), fs64.cpu().numpy().astype(np.float64), tag=f"prefill Q128 vs Q64 L{li}")
+        del fs64
         if li not in sample_layers:
             continue
         heads = (16 * (li % 8) + 3, 16 * (li % 8) + 5)  # two heads of one group
@@ -168,7 +178,10 @@ def test_long_prefill_27_layers_b4_T4096(m2):
         ref = oracle.mixer_scan(d, inp, heads=heads)
         yh = y[:, :, heads[0]:heads[1]].contiguous()
         yg = bf16_bits_to_f64(host(yh))
-        assert y_error(yg, ref["y"][:, :, heads[0]:heads[1]], "bf16") <= Y_TOL, li
-        assert state_error(fs[:, heads[0]:heads[1]].cpu().numpy(), ref["final_ssm"][:, heads[0]:heads[1]]) <= STATE_TOL, li
+        ybar = oracle.mixer_scan_magnitude(d, inp, heads=heads)
+        check_scan_y(yg, ref["y"][:, :, heads[0]:heads[1]], ybar[:, :, heads[0]:heads[1]], "bf16",
+                     tag=f"prefill y L{li}")
+        check_state(fs[:, heads[0]:heads[1]].cpu().numpy(), ref["final_ssm"][:, heads[0]:heads[1]],
+                    tag=f"prefill state L{li}")
         del dv, y, fs, fc
         torch.cuda.empty_cache()

@@ -249,6 +249,39 @@ def test_mixer_scan_composes_pinned_parts(oracle_lib):
     assert rel(r["final_ssm"], hq) < 1e-12
 
 
+def test_magnitude_equals_y_when_every_term_is_positive(oracle_lib):
+    """With every post-conv x~, B~, C~ positive (a conv bias of +4 against
+    pre-activations of spread ~0.6), D = 0 and a non-negative initial state,
+    no term of the recurrence is negative: the magnitude ybar equals y."""
+    d = Dims(H=4, P=6, N=5, G=2, K=4)
+    b, T = 2, 23
+    inp = mixer_inputs(21, d, b, T, "bf16")
+    inp["conv_b"] = np.full(d.CH, 4.0, np.float32)
+    inp["D"] = np.zeros(d.H, np.float32)
+    h0 = np.abs(ssm_state_inputs(22, d, b, scale=0.3).astype(np.float64))
+    r = oracle_lib.mixer_scan(d, inp, init_ssm=h0)
+    ybar = oracle_lib.mixer_scan_magnitude(d, inp, init_ssm=h0)
+    assert np.all(ybar > 0)
+    assert rel(ybar, r["y"]) < 1e-12
+
+
+def test_magnitude_bounds_the_state_space_part(oracle_lib):
+    """For signed inputs, |y - D x~| <= ybar everywhere (triangle inequality),
+    with equality nowhere near in general: it is a bound, not the value."""
+    d = Dims(H=4, P=6, N=5, G=2, K=4)
+    b, T = 2, 31
+    inp = mixer_inputs(23, d, b, T, "bf16")
+    ic = conv_state_inputs(24, d, b, "bf16")
+    h0 = ssm_state_inputs(25, d, b, scale=0.3).astype(np.float64)
+    no_d = dict(inp, D=np.zeros(d.H, np.float32))
+    ssm_part = oracle_lib.mixer_scan(d, no_d, init_ssm=h0, init_conv=ic)["y"]
+    ybar = oracle_lib.mixer_scan_magnitude(d, inp, init_ssm=h0, init_conv=ic)
+    assert np.all(np.abs(ssm_part) <= ybar * (1 + 1e-12))
+    assert np.median(np.abs(ssm_part) / ybar) < 0.9
+    # the magnitude covers the state-space terms only: D does not enter it
+    np.testing.assert_array_equal(ybar, oracle_lib.mixer_scan_magnitude(d, no_d, init_ssm=h0, init_conv=ic))
+
+
 @pytest.mark.parametrize("tsteps", [1, 2, 3, 4, 100])
 def test_step_equals_recompute(oracle_lib, tsteps):
     """Stepping t frames from zero caches == full-history recompute of t frames."""
