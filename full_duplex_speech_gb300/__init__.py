@@ -11,35 +11,9 @@ tensors (or raw device pointers) in, status codes checked, nothing computed
 in Python. Importing it loads the library; a missing library is an error,
 never a silent fallback.
 """
-from ._binding import (  # noqa: F401
-    M2Error,
-    M2Dims,
-    BF16,
-    F32,
-    library_path,
-    load,
-    dims,
-    mamba2_scan_workspace_bytes,
-    mamba2_conv_scan,
-    mamba2_conv_scan_varlen,
-    mamba2_scan_prepare_bc,
-    mamba2_scan_chunks,
-    mamba2_step_workspace_bytes,
-    mamba2_gated_norm,
-    mamba2_qlinear,
-    mamba2_attn_decode,
-    mamba2_attn_decode_workspace_bytes,
-    mamba2_step,
-    mamba2_step_noalloc,
-    mamba2_step_noalloc_max_bytes,
-    mamba2_status_string,
-    mamba2_last_cuda_error,
-    mamba2_device_error,
-)
+from . import _binding
+from ._binding import *  # noqa: F401,F403  (the C ABI's names, one for one)
 
-__all__ = [
-    "M2Error", "M2Dims", "BF16", "F32", "library_path", "load", "dims",
-    "mamba2_scan_workspace_bytes", "mamba2_conv_scan", "mamba2_conv_scan_varlen", "mamba2_scan_prepare_bc", "mamba2_scan_chunks", "mamba2_step_workspace_bytes", "mamba2_gated_norm", "mamba2_qlinear",
-    "mamba2_attn_decode", "mamba2_attn_decode_workspace_bytes",
-    "mamba2_step", "mamba2_step_noalloc", "mamba2_step_noalloc_max_bytes", "mamba2_status_string", "mamba2_last_cuda_error", "mamba2_device_error",
-]
+__all__ = [n for n in vars(_binding) if n.startswith("mamba2_")] + [
+    "M2Error", "M2Dims", "M2RowNorm", "M2Lm", "M2LmLayer", "BF16", "F32", "NORM_NONE", "NORM_RMS", "NORM_GATED",
+    "library_path", "load", "dims", "row_norm", "lm_model"]

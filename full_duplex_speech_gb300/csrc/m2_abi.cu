@@ -5,6 +5,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/mamba2.h"
 #include "m2_launch.h"
 
@@ -19,6 +21,9 @@ constexpr int kMaxDevices = 64;
 // Per-device facts resolved once: 0 = unknown, 1 = sm_103, 2 = other.
 int g_dev_kind[kMaxDevices] = {0};
 unsigned int* g_dev_error_ptr[kMaxDevices] = {nullptr};
+// Guards the per-device set-up above: two host threads making their first
+// call on one device must not see the kind set before the pointer.
+std::mutex g_dev_mutex;
 
 m2_status cuda_fail(cudaError_t e) {
     g_last_cuda_error = (int)e;
@@ -29,6 +34,7 @@ m2_status current_device(int* dev) {
     cudaError_t e = cudaGetDevice(dev);
     if (e != cudaSuccess) return cuda_fail(e);
     if (*dev < 0 || *dev >= kMaxDevices) return M2_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
     if (g_dev_kind[*dev] == 0) {
         int major = 0, minor = 0;
         e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev);
@@ -75,6 +81,31 @@ m2::Shape shape_of(const m2_dims* d) {
 
 namespace m2 {
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
+m2_status check_step_args(const m2_dims* d, int n_sessions, const void* x, const void* B, const void* C,
+                          const void* dt_raw, const float* A_log, const float* D, const float* dt_bias,
+                          const float* conv_w, const float* conv_b, const float* ssm_state,
+                          const void* conv_state, const void* y) {
+    m2_status st = check_dims(d, false);
+    if (st != M2_OK) return st;
+    if (n_sessions < 0) return M2_EINVAL;
+    const void* ptrs[] = {x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, ssm_state, conv_state, y};
+    for (const void* p : ptrs)
+        if (!p) return M2_EINVAL;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return M2_EALIGN;
+    return M2_OK;
+}
+
+m2_status check_device() {
+    int dev = 0;
+    return current_device(&dev);
+}
+
+unsigned int* device_error_word() {
+    int dev = 0;
+    return current_device(&dev) == M2_OK ? g_dev_error_ptr[dev] : nullptr;
+}
 }  // namespace m2
 
 extern "C" {
@@ -110,29 +141,107 @@ m2_status mamba2_device_error(void* stream, unsigned int* code) {
     return e == cudaSuccess ? M2_OK : cuda_fail(e);
 }
 
-m2_status mamba2_qlinear(int rows, int in_features, int out_features, int group_size, int bits, const void* x,
-                         const uint32_t* wq, const void* scales, const void* biases, void* y, void* stream) {
+}  // extern "C"
+
+namespace {
+
+bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+
+// Checks a row norm for rows of `in` inputs and fills `n` (kind 0 for NULL).
+m2_status row_norm_setup(const m2_row_norm* norm, int in, m2::RowNorm* n) {
+    n->kind = 0;
+    n->weight = nullptr;
+    n->eps = 0.f;
+    n->groups = 1;
+    n->gate = nullptr;
+    n->gate_stride = 0;
+    if (!norm || norm->kind == M2_NORM_NONE) return M2_OK;
+    if (norm->kind != M2_NORM_RMS && norm->kind != M2_NORM_GATED) return M2_EINVAL;
+    if (!norm->weight || !(norm->eps >= 0.f) || !(norm->eps < INFINITY)) return M2_EINVAL;
+    if (!aligned16(norm->weight)) return M2_EALIGN;
+    n->kind = norm->kind == M2_NORM_RMS ? 1 : 2;
+    n->weight = norm->weight;
+    n->eps = norm->eps;
+    if (in % 32 != 0) return M2_ESHAPE;
+    if (n->kind == 2) {
+        if (!norm->gate || norm->groups <= 0 || norm->gate_stride < in) return M2_EINVAL;
+        if (norm->groups > m2::kMaxNormGroups || in % norm->groups != 0 || (in / norm->groups) % 32 != 0)
+            return M2_ESHAPE;
+        if (!aligned16(norm->gate) || (norm->gate_stride * 2) % 16 != 0) return M2_EALIGN;
+        n->groups = norm->groups;
+        n->gate = norm->gate;
+        n->gate_stride = norm->gate_stride;
+    }
+    return M2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+m2_status mamba2_qlinear_fused(int rows, int in_features, int out_features, int group_size, int bits,
+                               const void* x, long x_stride, const m2_row_norm* norm, const uint32_t* wq,
+                               const void* scales, const void* biases, const void* residual, void* y,
+                               void* stream) {
     if (rows < 0 || in_features <= 0 || out_features <= 0 || group_size <= 0 || bits <= 0) return M2_EINVAL;
     if (group_size != 64 || bits != 4) return M2_EUNSUPPORTED;
     if (in_features % 64 != 0 || in_features > m2::kQlMaxIn) return M2_ESHAPE;
-    if (!x || !wq || !scales || !biases || !y) return M2_EINVAL;
-    if (!aligned16(x) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
-        (reinterpret_cast<uintptr_t>(biases) & 1u) || (reinterpret_cast<uintptr_t>(y) & 1u))
+    if (!x || !wq || !scales || !biases || !y || x_stride < in_features) return M2_EINVAL;
+    if (!aligned16(x) || (x_stride * 2) % 16 != 0 || !aligned16(wq) || !aligned2(scales) || !aligned2(biases) ||
+        !aligned2(y) || !aligned2(residual))
         return M2_EALIGN;
+    m2::QLinearArgs a;
+    m2_status st = row_norm_setup(norm, in_features, &a.norm);
+    if (st != M2_OK) return st;
     int dev = 0;
-    m2_status st = current_device(&dev);
+    st = current_device(&dev);
     if (st != M2_OK) return st;
     if (rows == 0) return M2_OK;
-    m2::QLinearArgs a;
     a.rows = rows;
     a.in = in_features;
     a.out = out_features;
     a.x = x;
+    a.x_stride = x_stride;
     a.wq = wq;
     a.scales = static_cast<const uint16_t*>(scales);
     a.biases = static_cast<const uint16_t*>(biases);
+    a.residual = residual;
     a.y = y;
     cudaError_t e = m2::launch_qlinear(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M2_OK : cuda_fail(e);
+}
+
+m2_status mamba2_qlinear(int rows, int in_features, int out_features, int group_size, int bits, const void* x,
+                         const uint32_t* wq, const void* scales, const void* biases, void* y, void* stream) {
+    return mamba2_qlinear_fused(rows, in_features, out_features, group_size, bits, x, in_features, nullptr, wq,
+                                scales, biases, nullptr, y, stream);
+}
+
+m2_status mamba2_linear_bf16(int rows, int in_features, int out_features, const void* x, long x_stride,
+                             const m2_row_norm* norm, const void* w, const void* residual, void* y, long y_stride,
+                             void* stream) {
+    if (rows < 0 || in_features <= 0 || out_features <= 0) return M2_EINVAL;
+    if (in_features % 32 != 0 || in_features > m2::kLinMaxIn) return M2_ESHAPE;
+    if (!x || !w || !y || x_stride < in_features || y_stride < out_features) return M2_EINVAL;
+    if (!aligned16(x) || (x_stride * 2) % 16 != 0 || !aligned16(w) || !aligned2(y) || !aligned2(residual))
+        return M2_EALIGN;
+    m2::LinearArgs a;
+    m2_status st = row_norm_setup(norm, in_features, &a.norm);
+    if (st != M2_OK) return st;
+    int dev = 0;
+    st = current_device(&dev);
+    if (st != M2_OK) return st;
+    if (rows == 0) return M2_OK;
+    a.rows = rows;
+    a.in = in_features;
+    a.out = out_features;
+    a.x = x;
+    a.x_stride = x_stride;
+    a.w = w;
+    a.residual = residual;
+    a.y = y;
+    a.y_stride = y_stride;
+    cudaError_t e = m2::launch_linear_bf16(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M2_OK : cuda_fail(e);
 }
 
@@ -195,6 +304,10 @@ m2_status mamba2_attn_decode(int n_sessions, int n_heads, int n_kv_heads, int he
     a.out = out;
     a.ws = static_cast<float*>(workspace);
     a.err = g_dev_error_ptr[dev];
+    a.q_ss = (long)n_heads * head_dim;
+    a.kv_ss = (long)n_kv_heads * head_dim;
+    a.out_ss = (long)n_heads * head_dim;
+    a.len_add = 0;
     cudaError_t e = m2::launch_attn_decode(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M2_OK : cuda_fail(e);
 }
@@ -225,25 +338,24 @@ m2_status mamba2_gated_norm(const m2_dims* d, int rows, const void* y, const voi
     return e == cudaSuccess ? M2_OK : cuda_fail(e);
 }
 
-m2_status mamba2_step(const m2_dims* d, int n_sessions, const void* x, const void* B,
-                      const void* C, const void* dt_raw, const float* A_log, const float* D,
-                      const float* dt_bias, const float* conv_w, const float* conv_b,
-                      float* ssm_state, void* conv_state, void* y, void* workspace,
-                      size_t workspace_bytes, void* stream) {
-    m2_status st = check_dims(d, false);
+}  // extern "C"
+
+namespace {
+
+// mamba2_step and mamba2_step_strided: `sx`, `sbc`, `sdt` are the elements
+// from one session's row of x, of B and C, and of dt_raw to the next.
+m2_status step_impl(const m2_dims* d, int n_sessions, const void* x, const void* B, const void* C,
+                    const void* dt_raw, long sx, long sbc, long sdt, const float* A_log, const float* D,
+                    const float* dt_bias, const float* conv_w, const float* conv_b, float* ssm_state,
+                    void* conv_state, void* y, void* workspace, size_t workspace_bytes, void* stream) {
+    m2_status st = m2::check_step_args(d, n_sessions, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b,
+                                       ssm_state, conv_state, y);
     if (st != M2_OK) return st;
-    if (n_sessions < 0) return M2_EINVAL;
-    const void* ptrs[] = {x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, ssm_state, conv_state, y};
-    for (const void* p : ptrs)
-        if (!p) return M2_EINVAL;
-    for (const void* p : ptrs)
-        if (!aligned16(p)) return M2_EALIGN;
     const m2::Shape s = shape_of(d);
     const size_t need = m2::step_workspace_bytes(s, n_sessions);
     if (!workspace || workspace_bytes < need) return M2_EWORKSPACE;
     if (!aligned16(workspace)) return M2_EALIGN;
-    int dev = 0;
-    st = current_device(&dev);
+    st = m2::check_device();
     if (st != M2_OK) return st;
     if (n_sessions == 0) return M2_OK;
 
@@ -254,6 +366,9 @@ m2_status mamba2_step(const m2_dims* d, int n_sessions, const void* x, const voi
     a.B = B;
     a.C = C;
     a.dt_raw = dt_raw;
+    a.sx = sx;
+    a.sbc = sbc;
+    a.sdt = sdt;
     a.A_log = A_log;
     a.D = D;
     a.dt_bias = dt_bias;
@@ -267,6 +382,31 @@ m2_status mamba2_step(const m2_dims* d, int n_sessions, const void* x, const voi
                                        ((size_t)n_sessions * s.CH() * 4 + 255) / 256 * 256);
     cudaError_t e = m2::launch_step(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M2_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+m2_status mamba2_step(const m2_dims* d, int n_sessions, const void* x, const void* B,
+                      const void* C, const void* dt_raw, const float* A_log, const float* D,
+                      const float* dt_bias, const float* conv_w, const float* conv_b,
+                      float* ssm_state, void* conv_state, void* y, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    const long HP = d ? (long)d->nheads * d->headdim : 0, GN = d ? (long)d->ngroups * d->dstate : 0;
+    return step_impl(d, n_sessions, x, B, C, dt_raw, HP, GN, d ? d->nheads : 0, A_log, D, dt_bias, conv_w,
+                     conv_b, ssm_state, conv_state, y, workspace, workspace_bytes, stream);
+}
+
+m2_status mamba2_step_strided(const m2_dims* d, int n_sessions, const void* x, const void* B, const void* C,
+                              const void* dt_raw, long in_row_stride, const float* A_log, const float* D,
+                              const float* dt_bias, const float* conv_w, const float* conv_b, float* ssm_state,
+                              void* conv_state, void* y, void* workspace, size_t workspace_bytes, void* stream) {
+    if (d && (in_row_stride <= 0 ||
+              (in_row_stride * (d->act == M2_BF16 ? 2 : 4)) % 16 != 0))
+        return in_row_stride <= 0 ? M2_EINVAL : M2_EALIGN;
+    return step_impl(d, n_sessions, x, B, C, dt_raw, in_row_stride, in_row_stride, in_row_stride, A_log, D,
+                     dt_bias, conv_w, conv_b, ssm_state, conv_state, y, workspace, workspace_bytes, stream);
 }
 
 size_t mamba2_scan_workspace_bytes(const m2_dims* d, int chunk) {
@@ -327,6 +467,9 @@ m2_status scan_setup(const m2_dims* d, const void* x, const void* B, const void*
     a->ws_bytes = workspace_bytes;
     a->err = g_dev_error_ptr[dev];
     a->lens = nullptr;
+    a->fx = s.HP();
+    a->fbc = s.GN();
+    a->fdt = s.H;
     return M2_OK;
 }
 
@@ -372,6 +515,22 @@ m2_status mamba2_conv_scan_varlen(const m2_dims* d, const int* lengths, const vo
     m2_status st = scan_setup(M2_SCAN_ARGS, &a);
     if (st != M2_OK || d->batch == 0) return st;
     a.lens = lengths;
+    cudaError_t e = m2::launch_scan_prepare(a, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = m2::launch_scan_chunks(a, true, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? M2_OK : cuda_fail(e);
+}
+
+m2_status mamba2_conv_scan_strided(const m2_dims* d, const void* x, const void* B, const void* C, const void* dt_raw,
+                                   long in_row_stride, const float* A_log, const float* D, const float* dt_bias,
+                                   const float* conv_w, const float* conv_b, int chunk, const float* init_ssm,
+                                   const void* init_conv, void* y, float* final_ssm, void* final_conv,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    if (d && in_row_stride <= 0) return M2_EINVAL;
+    if (d && (in_row_stride * (d->act == M2_BF16 ? 2 : 4)) % 16 != 0) return M2_EALIGN;
+    m2::ScanArgs a;
+    m2_status st = scan_setup(M2_SCAN_ARGS, &a);
+    if (st != M2_OK || d->batch == 0) return st;
+    a.fx = a.fbc = a.fdt = in_row_stride;
     cudaError_t e = m2::launch_scan_prepare(a, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = m2::launch_scan_chunks(a, true, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M2_OK : cuda_fail(e);

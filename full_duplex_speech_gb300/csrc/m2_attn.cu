@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnArgs a) {
 
     pdl_wait();  // the inputs and the caches may come from the previous kernel
     pdl_trigger();
-    const int len = a.lens[s];
+    const int len = a.lens[s] + a.len_add;
     if (len < 0 || len >= a.Tmax) return;  // refused; the combine kernel reports it
     const int t0 = chunk * tc;
     if (t0 > len) return;                  // past this session's positions
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnArgs a) {
         if (tid < 2 * V16) {
             const int which = tid / V16, piece = tid % V16;
             const uint8_t* src = reinterpret_cast<const uint8_t*>(which ? a.v_new : a.k_new) +
-                                 ((size_t)s * a.Hkv + g) * RB + piece * 16;
+                                 (size_t)s * a.kv_ss * sizeof(TA) + (size_t)g * RB + piece * 16;
             const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
             *reinterpret_cast<uint4*>((which ? sV : sK) + (size_t)(len - t0) * RB + piece * 16) = v;
             uint8_t* dst = reinterpret_cast<uint8_t*>(which ? a.v_cache : a.k_cache) + (kvrow + len) * RB + piece * 16;
@@ -201,7 +201,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(AttnArgs a) {
     for (int r = 0; r < RM; ++r) {
         if (r < R) {
             Lane16<TA> qr;
-            qr.load_global(reinterpret_cast<const uint8_t*>(a.q) + ((size_t)s * a.Hq + g * R + r) * RB, i8);
+            qr.load_global(reinterpret_cast<const uint8_t*>(a.q) + (size_t)s * a.q_ss * sizeof(TA) +
+                               (size_t)(g * R + r) * RB, i8);
             qr.unpack(qf[r]);
         }
     }
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(kAttnMaxR * 64) attn_combine_kernel(AttnArgs a
     const int r = threadIdx.x >> 6, dp = threadIdx.x & 63, lane = threadIdx.x & 31;
     pdl_wait();  // the split kernel's partial results
     pdl_trigger();
-    const int len = a.lens[s];
+    const int len = a.lens[s] + a.len_add;
     const bool bad = len < 0 || len >= a.Tmax;  // the same for the whole block
     const int nch = attn_chunks(a.Tmax, tc);
     const int nc = bad ? 0 : len / tc + 1;  // chunks holding positions 0..len
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(kAttnMaxR * 64) attn_combine_kernel(AttnArgs a
     } else if (threadIdx.x == 0) {
         atomicOr(a.err, ERR_ATTN_LENGTH);
     }
-    const size_t o = ((size_t)s * a.Hq + g * R + r) * kAttnD + 2 * dp;
+    const size_t o = (size_t)s * a.out_ss + (size_t)(g * R + r) * kAttnD + 2 * dp;
     if constexpr (sizeof(TA) == 2) {
         const uint32_t w = (uint32_t)float_to_bf16_bits(v0) | ((uint32_t)float_to_bf16_bits(v1) << 16);
         *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(a.out) + o) = w;

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/mamba2.h"
+
 namespace m2 {
 
 struct Shape {
@@ -21,6 +23,9 @@ struct StepArgs {
     Shape s;
     int S;  // sessions
     const void *x, *B, *C, *dt_raw;
+    // elements from one session's row of x, of B and C, and of dt_raw to the
+    // next (dense: H*P, G*N, H; rows of one projection output: its width)
+    long sx, sbc, sdt;
     const float *A_log, *D, *dt_bias, *conv_w, *conv_b;
     float* ssm;
     void* conv;
@@ -36,6 +41,9 @@ struct ScanArgs {
     Shape s;
     int batch, T, chunk;
     const void *x, *B, *C, *dt_raw;
+    // elements from one frame's row of x, of B and C, and of dt_raw to the
+    // next (dense: H*P, G*N, H); sequence b starts at row b*T
+    long fx, fbc, fdt;
     const float *A_log, *D, *dt_bias, *conv_w, *conv_b;
     const float* init_ssm;
     const void* init_conv;
@@ -61,19 +69,52 @@ struct NormArgs {
 // Gated RMSNorm of the mixer output (y * silu(z), grouped RMS, weight).
 cudaError_t launch_gated_norm(const NormArgs& a, cudaStream_t st);
 
-// 4-bit affine group-quantized linear layer (group 64): y = x W^T.
+// How each row of a linear layer's input is formed before the product:
+// kind 0: x as it is; kind 1: RMSNorm of the whole row, x * weight /
+// sqrt(mean(x^2) + eps); kind 2: gated RMSNorm, v = x * silu(z) normalised
+// over `groups` contiguous blocks, v * weight / sqrt(mean_block(v^2) + eps).
+// The normalised row is rounded to bf16 (as a separate norm kernel would
+// store it) before it enters the product.
+constexpr int kMaxNormGroups = 64;
+struct RowNorm {
+    int kind;
+    const float* weight;  // [in] fp32 (kinds 1, 2)
+    float eps;
+    int groups;           // kind 2 (kind 1: 1)
+    const void* gate;     // kind 2: z, bf16, one row per row of x
+    long gate_stride;     // elements between rows of z
+};
+
+// 4-bit affine group-quantized linear layer (group 64): y = x W^T (+ residual).
 constexpr int kQlMaxIn = 16384;  // input features, at most
 struct QLinearArgs {
     int rows, in, out;
-    const void* x;            // [rows, in] bf16
+    const void* x;            // [rows, in] bf16, rows x_stride elements apart
+    long x_stride;
+    RowNorm norm;
     const uint32_t* wq;       // [out, in/8]: eight 4-bit fields per word, the first input lowest
     const uint16_t* scales;   // [out, in/64] bf16
     const uint16_t* biases;   // [out, in/64] bf16
+    const void* residual;     // NULL, or [rows, out] bf16 added before the rounding (may alias y)
     void* y;                  // [rows, out] bf16
 };
 // Rows of x the kernel takes per pass over the weights (0: `in` too large).
 int qlinear_rows_per_pass(int in);
 cudaError_t launch_qlinear(const QLinearArgs& a, cudaStream_t st);
+
+// Dense bf16 linear layer for the few rows of a decode step: y = x W^T (+ residual).
+constexpr int kLinMaxIn = 16384;
+struct LinearArgs {
+    int rows, in, out;
+    const void* x;        // [rows, in] bf16, rows x_stride elements apart
+    long x_stride;
+    RowNorm norm;
+    const void* w;        // [out, in] bf16
+    const void* residual; // NULL, or [rows, out] bf16 (may alias y)
+    void* y;              // [rows, out] bf16, rows y_stride elements apart
+    long y_stride;
+};
+cudaError_t launch_linear_bf16(const LinearArgs& a, cudaStream_t st);
 
 // One cached decode position of grouped-query attention with KV-cache append.
 constexpr int kAttnD = 128;     // head_dim
@@ -89,12 +130,28 @@ struct AttnArgs {
     float* ws;                  // per-chunk partial results
     unsigned int* err;          // device error word
     int tc;                     // positions per chunk (set by the launcher)
+    // elements from one session's q, k_new / v_new and out to the next's
+    // (dense: Hq*D, Hkv*D, Hq*D), and a count added to every length (the
+    // positions of a prefill after the first)
+    long q_ss, kv_ss, out_ss;
+    int len_add;
 };
 size_t attn_workspace_bytes(int S, int Hq, int Hkv, int Tmax, bool bf16);
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st);
 
 // Records a CUDA error for mamba2_last_cuda_error() on the calling thread.
 void record_cuda_error(cudaError_t e);
+
+// The argument checks of mamba2_step before its workspace check: dimensions,
+// session count, NULL and misaligned pointers (M2_OK when they pass).
+m2_status check_step_args(const m2_dims* d, int n_sessions, const void* x, const void* B, const void* C,
+                          const void* dt_raw, const float* A_log, const float* D, const float* dt_bias,
+                          const float* conv_w, const float* conv_b, const float* ssm_state,
+                          const void* conv_state, const void* y);
+// M2_OK when the current device is an sm_103 GPU (and its set-up is done).
+m2_status check_device();
+// The device error word of the current device (after check_device).
+unsigned int* device_error_word();
 
 size_t scan_workspace_bytes(const Shape& s, int batch, int T, int chunk);
 // B/C conv prologue into the workspace tiles (first half of a scan).

@@ -24,6 +24,7 @@
 
 #include "m2_common.cuh"
 #include "m2_launch.h"
+#include "m2_rowprep.cuh"
 
 namespace m2 {
 
@@ -89,32 +90,35 @@ __device__ __forceinline__ void load_batch(const QLinearArgs& a, int o, int bi, 
 }
 
 // NB rows of x per pass over the weights.
-template <int NB>
+template <int NB, int KIND, bool RES>
 __global__ void __launch_bounds__(kQlThreads, 1) qlinear_kernel(QLinearArgs a) {
     extern __shared__ float4 ql_smem4[];
     const int in = a.in, nchunks = in / kChunk, ngroups = in / kGroup;
     uint32_t* sx = reinterpret_cast<uint32_t*>(ql_smem4);                        // [NB][nchunks][kChunkPitch]
     float* ssum = reinterpret_cast<float*>(sx + (size_t)NB * nchunks * kChunkPitch);  // [NB][nchunks]
+    float* srs = ssum + (size_t)NB * nchunks;                                    // [NB][norm groups]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gwarp = blockIdx.x * kQlWarps + warp, nwarps = gridDim.x * kQlWarps;
-    const uint16_t* xb = reinterpret_cast<const uint16_t*>(a.x);
     uint16_t* yb = reinterpret_cast<uint16_t*>(a.y);
+    const uint16_t* rb = reinterpret_cast<const uint16_t*>(a.residual);
 
-    pdl_wait();  // x may come from the previous kernel
+    pdl_wait();  // x (and z, the residual) may come from the previous kernel
     for (int r0 = 0; r0 < a.rows; r0 += NB) {
         const int nr = min(NB, a.rows - r0);
+        // the norm's scales of this pass's rows (ssum serves as scratch)
+        if (KIND != 0) rowprep::norm_scales<kQlThreads, KIND>(a.x, a.x_stride, a.norm, in, r0, nr, NB, ssum, srs);
         // stage x as the bf16 pairs of each word, (x_k, x_{k+4}), and the fp32
         // sum of x over each chunk
         for (int e = tid; e < NB * nchunks; e += kQlThreads) {
             const int r = e / nchunks, c = e % nchunks;
+            uint32_t wd[16];
+            rowprep::staged32<KIND>(a.x, a.x_stride, a.norm, in, r0, r, nr, c * kChunk, srs, wd);
             float s = 0.f;
             uint4* dst = reinterpret_cast<uint4*>(sx + ((size_t)r * nchunks + c) * kChunkPitch);
-            const uint4* src = reinterpret_cast<const uint4*>(xb + (size_t)(r0 + min(r, nr - 1)) * in + c * kChunk);
 #pragma unroll
             for (int v = 0; v < kChunk / 8; ++v) {
-                uint4 u = make_uint4(0, 0, 0, 0);  // rows past the last of x count as zero
-                if (r < nr) u = __ldg(src + v);
-                // u holds x_0..x_7 of word v as (x0 x1) (x2 x3) (x4 x5) (x6 x7)
+                // word v holds x_0..x_7 as (x0 x1) (x2 x3) (x4 x5) (x6 x7)
+                const uint4 u = make_uint4(wd[4 * v], wd[4 * v + 1], wd[4 * v + 2], wd[4 * v + 3]);
                 dst[v] = make_uint4(__byte_perm(u.x, u.z, 0x5410), __byte_perm(u.x, u.z, 0x7632),
                                     __byte_perm(u.y, u.w, 0x5410), __byte_perm(u.y, u.w, 0x7632));
                 const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
@@ -171,8 +175,13 @@ __global__ void __launch_bounds__(kQlThreads, 1) qlinear_kernel(QLinearArgs a) {
                 }
                 if (lane == 0) {
 #pragma unroll
-                    for (int r = 0; r < NB; ++r)
-                        if (r < nr) yb[(size_t)(r0 + r) * a.out + o] = float_to_bf16_bits(acc[r]);
+                    for (int r = 0; r < NB; ++r) {
+                        if (r < nr) {
+                            const size_t i = (size_t)(r0 + r) * a.out + o;
+                            const float res = RES ? bf16_bits_to_float(rb[i]) : 0.f;
+                            yb[i] = float_to_bf16_bits(acc[r] + res);
+                        }
+                    }
                 }
 #pragma unroll
                 for (int r = 0; r < NB; ++r) acc[r] = 0.f;
@@ -192,10 +201,12 @@ __global__ void __launch_bounds__(kQlThreads, 1) qlinear_kernel(QLinearArgs a) {
 
 constexpr int kQlSmemCap = 128 * 1024;  // shared memory of one pass: x as fp32 and its chunk sums
 
-size_t smem_bytes(int nb, int in) { return (size_t)nb * (in / kChunk) * (kChunkPitch + 1) * sizeof(uint32_t); }
+size_t smem_bytes(int nb, int in) {
+    return ((size_t)nb * (in / kChunk) * (kChunkPitch + 1) + (size_t)nb * kMaxNormGroups) * sizeof(uint32_t);
+}
 
-template <int NB>
-cudaError_t launch_nb(const QLinearArgs& a, cudaStream_t st) {
+template <int NB, int KIND, bool RES>
+cudaError_t launch_variant(const QLinearArgs& a, cudaStream_t st) {
     const size_t smem = smem_bytes(NB, a.in);
     static int configured_device = -1;
     int dev = 0, sms = 0;
@@ -203,13 +214,25 @@ cudaError_t launch_nb(const QLinearArgs& a, cudaStream_t st) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(qlinear_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQlSmemCap);
+        e = cudaFuncSetAttribute(qlinear_kernel<NB, KIND, RES>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQlSmemCap);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
     const long want = ((long)a.out + kQlWarps - 1) / kQlWarps;
     const int blocks = (int)(want < sms ? want : (long)sms);
-    return launch_pdl(qlinear_kernel<NB>, dim3(blocks), dim3(kQlThreads), smem, st, a);
+    return launch_pdl(qlinear_kernel<NB, KIND, RES>, dim3(blocks), dim3(kQlThreads), smem, st, a);
+}
+
+// The kernel variant for this norm kind and residual.
+template <int NB>
+cudaError_t launch_nb(const QLinearArgs& a, cudaStream_t st) {
+    const bool res = a.residual != nullptr;
+    switch (a.norm.kind) {
+        case 0: return res ? launch_variant<NB, 0, true>(a, st) : launch_variant<NB, 0, false>(a, st);
+        case 1: return res ? launch_variant<NB, 1, true>(a, st) : launch_variant<NB, 1, false>(a, st);
+        case 2: return res ? launch_variant<NB, 2, true>(a, st) : launch_variant<NB, 2, false>(a, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace

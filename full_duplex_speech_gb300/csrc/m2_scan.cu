@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nch
             have[k] = in_seq || from_tail;
             const void* base = from_tail ? a.init_conv : src;
             const size_t elem = from_tail ? ((size_t)b * (s.K - 1) + (s.K - 1 + t)) * CH + ch0
-                                          : (((size_t)b * T + (in_seq ? t : c0)) * s.G + g) * s.N + n0;
+                                          : ((size_t)b * T + (in_seq ? t : c0)) * a.fbc + (size_t)g * s.N + n0;
             v[k].load_pinned(base, elem);
         }
 #pragma unroll
@@ -179,8 +179,8 @@ __device__ void write_tail(const ScanArgs& a, int b, long c) {
         size_t elem;
         if (t >= 0) {
             base = c < HP ? a.x : (c < HP + GN ? a.B : a.C);
-            elem = c < HP ? ((size_t)b * T + t) * HP + c
-                          : ((size_t)b * T + t) * GN + (c < HP + GN ? c - HP : c - HP - GN);
+            elem = c < HP ? ((size_t)b * T + t) * a.fx + c
+                          : ((size_t)b * T + t) * a.fbc + (c < HP + GN ? c - HP : c - HP - GN);
         } else {
             base = a.init_conv;
             elem = ((size_t)b * 3 + (3 + t)) * CH + c;
@@ -237,8 +237,8 @@ struct SsdSmem {
     static constexpr uint32_t kWsum = kTj + 512;          // float warp sums[8]
     static constexpr uint32_t kCw = kWsum + 64;           // float conv_w[P][4]
     static constexpr uint32_t kCb = kCw + P * 16;         // float conv_b[P]
-    static constexpr uint32_t kBar = (kCb + P * 4 + 15) / 16 * 16;  // 8 mbarriers
-    static constexpr uint32_t kTmem = kBar + 64;          // TMEM base address
+    static constexpr uint32_t kBar = (kCb + P * 4 + 15) / 16 * 16;  // 9 mbarriers
+    static constexpr uint32_t kTmem = kBar + 72;          // TMEM base address
     static constexpr uint32_t kFlag = kTmem + 4;          // abort flag
     static constexpr uint32_t kBytes = kFlag + 4 + 1024;  // + slack to align the base to 1024
 };
@@ -306,6 +306,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     uint64_t* bar_y = bar_a + 5;                                   // every MMA of the chunk done
     uint64_t* bar_op1 = bar_a + 6;                                 // phase-1 operands written (256 arrivals)
     uint64_t* bar_op2 = bar_a + 7;                                 // phase-2 operands written (256 arrivals)
+    uint64_t* bar_end = bar_a + 8;                                 // MMAs of an abandoned chunk done
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::kTmem);
     volatile uint32_t* sFlag = reinterpret_cast<uint32_t*>(sm + L::kFlag);
 
@@ -326,6 +327,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         tc::mbar_init(bar_y, 1);
         tc::mbar_init(bar_op1, kComputeThreads);
         tc::mbar_init(bar_op2, kComputeThreads);
+        tc::mbar_init(bar_end, 1);
         tc::fence_mbar_init();
         *sFlag = 0;
     }
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     const float dtb = ldg_pinned_f32(a.dt_bias + h);
     ActRaw<TA> dt_raw_bits = 0;
     if (compute && nchb > 0 && half == 0 && row < min(Q, Tb))
-        dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + row) * s.H + h);
+        dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + row) * a.fdt + h);
     if (tid < P) {
         reinterpret_cast<float4*>(sCw)[tid] = cw;
         sCb[tid] = cb;
@@ -466,7 +468,13 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 }
             }
             if (*sFlag) {
-                // a wait gave up: let copies still in flight land before the CTA exits
+                // A wait gave up. Before the CTA frees TMEM and exits: every MMA
+                // this thread issued must be done (the commit arrives on bar_end
+                // once all of them have completed; some, such as Y_off and the
+                // state terms, are covered by no other commit), and the copies
+                // still in flight must land. Every wait here is bounded.
+                tc::mma_commit(bar_end);
+                tc::mbar_wait(bar_end, 0, 100000000ull);
                 for (int i = 0; i < 3; ++i) {
                     tc::mbar_wait(bar_a + i, 0, 100000000ull);
                     tc::mbar_wait(bar_a + i, 1, 100000000ull);
@@ -588,7 +596,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             dt_phase(min(Q, Tb), raw_to_f32<TA>(dt_raw_bits));
             dt_raw_bits = 0;
             if (half == 0 && nchb > 1 && row < min(Q, Tb - Q))
-                dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + Q + row) * s.H + h);
+                dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + Q + row) * a.fdt + h);
         }
 
         // The chunk loop is skewed so that CUDA-core work overlaps the tensor
@@ -791,7 +799,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 dt_phase(Ln, raw_to_f32<TA>(dt_raw_bits));
                 dt_raw_bits = 0;
                 if (half == 0 && row < Lnn)
-                    dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + c0 + 2 * Q + row) * s.H + h);
+                    dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + c0 + 2 * Q + row) * a.fdt + h);
             }
             wait_ok(bar_y, par, ERR_MBAR_TIMEOUT_MMA);
             tc::tc_fence_after();
@@ -847,7 +855,9 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// x viewed as a 3-D tensor [b][T][H*P] (innermost last); a box is the
+// x viewed as a 3-D tensor [b][T][H*P] (innermost last; rows fx elements
+// apart, which is H*P for a dense x and wider for x inside the rows of a
+// projection output); a box is the
 // [kRawRows x (P + pad)] pre-conv rows of one head for one chunk (the pad
 // channels belong to the next head, or lie past the end and read as zero).
 template <typename TA, int P>
@@ -856,7 +866,8 @@ cudaError_t make_x_map(const ScanArgs& a, CUtensorMap* map) {
     if (!enc) return cudaErrorNotSupported;
     const cuuint64_t HP = (cuuint64_t)a.s.H * P;
     const cuuint64_t dims[3] = {HP, (cuuint64_t)a.T, (cuuint64_t)a.batch};
-    const cuuint64_t strides[2] = {HP * sizeof(TA), HP * (cuuint64_t)a.T * sizeof(TA)};
+    const cuuint64_t fx = (cuuint64_t)a.fx;
+    const cuuint64_t strides[2] = {fx * sizeof(TA), fx * (cuuint64_t)a.T * sizeof(TA)};
     const cuuint32_t box[3] = {(cuuint32_t)(P + SsdSmem<TA, P>::kRawPad), (cuuint32_t)kRawRows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapDataType dt = sizeof(TA) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;

@@ -79,11 +79,11 @@ __global__ void __launch_bounds__(kConvThreads) step_conv_kernel(StepArgs a) {
         // this frame's pre-conv input for channels [c, c+8)
         Act8<TA> cur;
         if (c < HP)
-            cur.load(a.x, (size_t)ses * HP + c);
+            cur.load(a.x, (size_t)ses * a.sx + c);
         else if (c < HP + GN)
-            cur.load(a.B, (size_t)ses * GN + (c - HP));
+            cur.load(a.B, (size_t)ses * a.sbc + (c - HP));
         else
-            cur.load(a.C, (size_t)ses * GN + (c - HP - GN));
+            cur.load(a.C, (size_t)ses * a.sbc + (c - HP - GN));
         Act8<TA> tail[3];
         load_tail<TA>(a, ses, c, tail);
         float out[8];
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kConvThreads) step_conv_kernel(StepArgs a) {
         shift_tail<TA>(a, ses, c, tail, cur);
     } else if (v - nvec < s.H) {
         const int h = (int)(v - nvec);
-        const float z = load_act<TA>(a.dt_raw, (size_t)ses * s.H + h) + __ldg(a.dt_bias + h);
+        const float z = load_act<TA>(a.dt_raw, (size_t)ses * a.sdt + h) + __ldg(a.dt_bias + h);
         a.ws_dt[(size_t)ses * s.H + h] = softplus_f32(z);
     }
 }

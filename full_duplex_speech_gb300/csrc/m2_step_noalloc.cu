@@ -12,7 +12,9 @@
 // The scratch is a file-scope __device__ array of kScratchBytes (1 MiB); every
 // GPU that loads the library holds it until the process exits. Its device
 // address is looked up once per device (cudaGetSymbolAddress, with that device
-// current) on the first call made there. All calls share it.
+// current) on the first call made there, and kept for the life of the process:
+// calls after a cudaDeviceReset of that device are not supported. All calls
+// share it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -40,9 +42,17 @@ m2_status mamba2_step_noalloc(const m2_dims* d, int n_sessions, const void* x, c
                               const void* C, const void* dt_raw, const float* A_log, const float* D,
                               const float* dt_bias, const float* conv_w, const float* conv_b,
                               float* ssm_state, void* conv_state, void* y, void* stream) {
-    // Size first: a request that does not fit is refused before touching the GPU.
+    // The checks of mamba2_step come first and in its order (arguments, then
+    // the size in place of its workspace check, then the device), so a NULL
+    // pointer or a GPU other than sm_103 gives the status it gives there. A
+    // request that does not fit is refused before touching the GPU.
+    m2_status st = m2::check_step_args(d, n_sessions, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b,
+                                       ssm_state, conv_state, y);
+    if (st != M2_OK) return st;
     const size_t need = mamba2_step_workspace_bytes(d, n_sessions);
     if (need > kScratchBytes) return M2_EWORKSPACE;
+    st = m2::check_device();
+    if (st != M2_OK) return st;
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -67,9 +77,8 @@ m2_status mamba2_step_noalloc(const m2_dims* d, int n_sessions, const void* x, c
         }
         scratch = g_scratch_ptr[dev];
     }
-    // Everything else (arguments, shapes, alignment, device) is validated by
-    // mamba2_step. The scratch needs no clearing: the step writes every byte it
-    // later reads within the same call.
+    // The scratch needs no clearing: the step writes every byte it later reads
+    // within the same call.
     return mamba2_step(d, n_sessions, x, B, C, dt_raw, A_log, D, dt_bias, conv_w, conv_b, ssm_state,
                        conv_state, y, scratch, kScratchBytes, stream);
 }

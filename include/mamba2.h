@@ -37,6 +37,11 @@
  *           already running surface at the caller's next synchronisation, as
  *           for any CUDA work. Device-side waits are bounded: a wait that
  *           runs out records a code readable with mamba2_device_error().
+ * Devices. The library looks up, once per device and on the first call
+ *           made there, the device addresses of its own device variables
+ *           (the error word; the scratch of mamba2_step_noalloc) and keeps
+ *           them for the life of the process. Calls on a device after a
+ *           cudaDeviceReset of it are not supported.
  * Layouts.  Contiguous, innermost index last:
  *             x [b,T,H,P]   B, C [b,T,G,N]   dt_raw [b,T,H]   y [b,T,H,P]
  *             ssm state [b,H,P,N] fp32
@@ -133,6 +138,23 @@ m2_status mamba2_conv_scan_varlen(const m2_dims* d, const int* lengths, const vo
                                   const float* init_ssm, const void* init_conv, void* y, float* final_ssm,
                                   void* final_conv, void* workspace, size_t workspace_bytes, void* stream);
 
+/* mamba2_conv_scan on inputs that are column slices of wider rows: the x, B,
+ * C and dt_raw of frame t of sequence b start in_row_stride * (b*T + t)
+ * elements past the x, B, C and dt_raw pointers. That is the layout of the
+ * Mamba layer's input projection output, one row per frame holding
+ * z | x | B | C | dt (VoiceChat issue, section config.json / text_config:
+ * the mixer's in_proj), so x = proj + H*P, B = proj + 2*H*P,
+ * C = B + G*N, dt_raw = C + G*N and in_row_stride = 2*H*P + 2*G*N + H (22656
+ * at the Nemotron-H shape) read the frame straight from it.
+ * in_row_stride > 0 (M2_EINVAL), and in_row_stride times the element size a
+ * multiple of 16 bytes (M2_EALIGN). Everything else is mamba2_conv_scan's:
+ * with in_row_stride equal to the dense widths the results are identical. */
+m2_status mamba2_conv_scan_strided(const m2_dims* d, const void* x, const void* B, const void* C, const void* dt_raw,
+                                   long in_row_stride, const float* A_log, const float* D, const float* dt_bias,
+                                   const float* conv_w, const float* conv_b, int chunk, const float* init_ssm,
+                                   const void* init_conv, void* y, float* final_ssm, void* final_conv,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* The two halves of mamba2_conv_scan, with the same arguments, for callers
  * that schedule or time them separately. mamba2_conv_scan(args) is exactly
  * mamba2_scan_prepare_bc(args) followed by mamba2_scan_chunks(args) on the
@@ -203,6 +225,63 @@ m2_status mamba2_gated_norm(const m2_dims* d, int rows, const void* y, const voi
 m2_status mamba2_qlinear(int rows, int in_features, int out_features, int group_size, int bits, const void* x,
                          const uint32_t* wq, const void* scales, const void* biases, void* y, void* stream);
 
+/* The norm that precedes a linear layer in the Nemotron-H blocks, fused into
+ * the layer's staging of its input rows (VoiceChat issue, section
+ * config.json / text_config: layer_norm_epsilon 1e-5, n_groups 8):
+ *   M2_NORM_RMS   (the pre-norm of every block):
+ *                   x' = weight * x / sqrt(mean over the row of x^2 + eps)
+ *   M2_NORM_GATED (the gated output norm of a Mamba layer, as
+ *                   mamba2_gated_norm): v = x * silu(z),
+ *                   x' = weight * v / sqrt(mean over each of `groups`
+ *                   contiguous blocks of v^2 + eps)
+ * computed in fp32 and rounded once to bf16 (what a separate norm kernel
+ * would store) before the product. weight: [in_features] fp32, 16-byte
+ * aligned. gate: z, bf16, one row per row of x, gate_stride elements apart
+ * (a multiple of 8, at least in_features), 16-byte aligned. groups: at most
+ * 64, dividing in_features into blocks of a multiple of 32 inputs. */
+typedef enum { M2_NORM_NONE = 0, M2_NORM_RMS = 1, M2_NORM_GATED = 2 } m2_norm_kind;
+typedef struct {
+    m2_norm_kind kind;
+    const float* weight;
+    float eps;
+    int groups;        /* M2_NORM_GATED only */
+    const void* gate;  /* M2_NORM_GATED only */
+    long gate_stride;  /* M2_NORM_GATED only */
+} m2_row_norm;
+
+/* mamba2_qlinear with the Mamba layer's neighbours fused in:
+ *   x rows x_stride elements apart (a multiple of 8, at least in_features);
+ *   norm (NULL or M2_NORM_NONE: none) applied to each row of x first: the
+ *     block's pre-norm before in_proj, the gated output norm before out_proj;
+ *   residual (NULL: none): [rows, out_features] bf16 added to the product
+ *     before its one rounding, y = residual + x' W^T; may alias y (the
+ *     residual stream updated in place).
+ * Errors as mamba2_qlinear, and M2_EINVAL / M2_ESHAPE / M2_EALIGN for a bad
+ * norm. With x_stride = in_features and no norm or residual the results are
+ * mamba2_qlinear's. */
+m2_status mamba2_qlinear_fused(int rows, int in_features, int out_features, int group_size, int bits,
+                               const void* x, long x_stride, const m2_row_norm* norm, const uint32_t* wq,
+                               const void* scales, const void* biases, const void* residual, void* y,
+                               void* stream);
+
+/* Dense bf16 linear layer for the few rows of a decode step: the attention
+ * layers' q|k|v and output projections, which the VoiceChat checkpoints keep
+ * in bf16 (VoiceChat issue, section config.json: only the embedding, the
+ * heads and the mixer projections are quantized; attention_bias false).
+ *     y[r][o] = residual[r][o] + sum_i w[o][i] x'[r][i]
+ * with x' the (optionally normalised) row of x, fp32 sums, one rounding.
+ * x: [rows, in_features] bf16, rows x_stride elements apart (a multiple of 8,
+ *   at least in_features), 16-byte aligned. w: [out_features, in_features]
+ *   bf16, 16-byte aligned. y, residual (NULL: none): rows y_stride elements
+ *   apart (at least out_features); residual may alias y; y must not alias x.
+ * Sizes: in_features a multiple of 32, at most 16384; rows >= 0 (rows == 0 is
+ *   a no-op once the arguments check out). Each pass over the weights takes
+ *   up to 8 rows of x.
+ * Errors: M2_EINVAL, M2_ESHAPE, M2_EALIGN, M2_EUNSUPPORTED, M2_ECUDA. */
+m2_status mamba2_linear_bf16(int rows, int in_features, int out_features, const void* x, long x_stride,
+                             const m2_row_norm* norm, const void* w, const void* residual, void* y, long y_stride,
+                             void* stream);
+
 /* One cached decode position of the hybrid model's grouped-query attention
  * layers, with the KV-cache append: the Nemotron-H attention layers (VoiceChat
  * issue, section config.json / text_config: num_attention_heads 40,
@@ -265,6 +344,18 @@ m2_status mamba2_step(const m2_dims* d, int n_sessions, const void* x, const voi
                       float* ssm_state, void* conv_state, void* y, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/* mamba2_step on inputs that are column slices of wider rows, one row per
+ * session: session s's x, B, C and dt_raw start in_row_stride * s elements
+ * past the x, B, C and dt_raw pointers (for instance the rows of the Mamba
+ * layer's input projection output z | x | B | C | dt, see
+ * mamba2_conv_scan_strided). in_row_stride > 0 (M2_EINVAL) and in_row_stride
+ * times the element size a multiple of 16 bytes (M2_EALIGN); everything else
+ * is mamba2_step's. */
+m2_status mamba2_step_strided(const m2_dims* d, int n_sessions, const void* x, const void* B, const void* C,
+                              const void* dt_raw, long in_row_stride, const float* A_log, const float* D,
+                              const float* dt_bias, const float* conv_w, const float* conv_b, float* ssm_state,
+                              void* conv_state, void* y, void* workspace, size_t workspace_bytes, void* stream);
+
 /* mamba2_step without a caller-provided workspace, for callers that cannot
  * allocate device memory: a real-time frame loop that must not call
  * cudaMalloc (it can synchronise the device mid-frame), a host that hands the
@@ -283,7 +374,9 @@ m2_status mamba2_step(const m2_dims* d, int n_sessions, const void* x, const voi
  * overlap on the GPU (on different streams, or from different host threads
  * without ordering) race on it and give undefined results; calls ordered on
  * one stream are safe. Nothing in it needs clearing between calls. Arguments,
- * results and every other error are those of mamba2_step. */
+ * results and every other error are those of mamba2_step, checked in the
+ * same order before the size (a NULL pointer is M2_EINVAL, another GPU
+ * M2_EUNSUPPORTED). */
 m2_status mamba2_step_noalloc(const m2_dims* d, int n_sessions, const void* x, const void* B,
                               const void* C, const void* dt_raw, const float* A_log, const float* D,
                               const float* dt_bias, const float* conv_w, const float* conv_b,
@@ -291,6 +384,87 @@ m2_status mamba2_step_noalloc(const m2_dims* d, int n_sessions, const void* x, c
 
 /* Size in bytes of the fixed scratch used by mamba2_step_noalloc. */
 size_t mamba2_step_noalloc_max_bytes(void);
+
+/* ------------------------------------------------------------------------
+ * One cached position of the hybrid language model, and its full-history
+ * recompute. The Nemotron-H model of VoiceChat interleaves Mamba ('M') and
+ * attention ('*') blocks (VoiceChat issue, section config.json /
+ * text_config: hybrid_override_pattern; its 27 'M' and 4 '*' layers; the 25
+ * MLP ('-') layers are not part of this library); the session keeps each
+ * Mamba layer's SSM state and conv tail and each attention layer's KV caches
+ * across positions ("docs/nemotron-voicechat.md", section Online session),
+ * and stepping positions from these caches gives the tokens a full-history
+ * recompute gives (same doc, section Offline timeline).
+ *
+ * Per block, on the residual stream h (bf16):
+ *   'M': proj = in_proj(RMSNorm(h))         z | x | B | C | dt per row
+ *        y    = mixer core (mamba2_step / mamba2_conv_scan) on x, B, C, dt
+ *        h    = h + out_proj(gated_norm(y, z))
+ *   '*': qkv  = [Wq; Wk; Wv] RMSNorm(h)      bf16 projections, no bias
+ *        o    = attention (mamba2_attn_decode) with the KV-cache append
+ *        h    = h + Wo o
+ * in_proj and out_proj are 4-bit group-64 (mamba2_qlinear layout); the norms
+ * and the residual adds are fused into the projections (m2_row_norm). Every
+ * activation stored between kernels is bf16, each computed in fp32 and
+ * rounded once. The final norm and the heads are not part of this call. */
+typedef struct {
+    const float* norm_w;          /* [hidden] fp32: the block's pre-norm */
+    /* 'M' blocks */
+    const uint32_t* in_wq;        /* in_proj [2*H*P + 2*G*N + H, hidden], 4-bit */
+    const void* in_scales;        /* [.., hidden/64] bf16 */
+    const void* in_biases;
+    const float *A_log, *D, *dt_bias, *conv_w, *conv_b;  /* the mixer core's, as mamba2_step */
+    const float* gnorm_w;         /* [H*P] fp32: the gated output norm */
+    const uint32_t* out_wq;       /* out_proj [hidden, H*P], 4-bit */
+    const void* out_scales;
+    const void* out_biases;
+    float* ssm_state;             /* [S,H,P,N] fp32, updated in place */
+    void* conv_state;             /* [S,K-1,CH] bf16, updated in place */
+    /* '*' blocks */
+    const void* wqkv;             /* [(n_heads + 2 n_kv_heads) * head_dim, hidden] bf16 */
+    const void* wo;               /* [hidden, n_heads * head_dim] bf16 */
+    void* k_cache;                /* [S, n_kv_heads, max_len, head_dim] bf16, updated at the new slots */
+    void* v_cache;
+} m2_lm_layer;
+
+typedef struct {
+    int n_layers;
+    const char* kinds;            /* n_layers characters, 'M' or '*' */
+    const m2_lm_layer* layers;    /* host array of n_layers */
+    int hidden;                   /* residual width (4480 in Nemotron-H) */
+    m2_dims mixer;                /* the mixer core's dims (batch, T ignored; act M2_BF16) */
+    int n_heads, n_kv_heads, head_dim, max_len;  /* attention blocks (40, 8, 128) */
+    float norm_eps;               /* all norms (1e-5) */
+    float attn_scale;             /* softmax scale (1/sqrt(head_dim)) */
+} m2_lm;
+
+/* Bytes of device scratch mamba2_lm_prefill needs for S sessions of T
+ * positions with this chunk length (mamba2_lm_step: T = 1, chunk ignored);
+ * 0 if the model description is invalid. */
+size_t mamba2_lm_workspace_bytes(const m2_lm* m, int n_sessions, int T, int chunk);
+
+/* One cached position for S sessions: hidden [S, hidden] bf16 holds the
+ * position's input (the fused embedding) and receives the residual stream
+ * after the last block. lengths [S] int32 in device memory: positions
+ * already in the KV caches (read on the device; the caller advances them
+ * by one after the call). Every Mamba block runs mamba2_step on its rows of
+ * the in_proj output (strided), every attention block mamba2_attn_decode.
+ * All host arrays (m, m->kinds, m->layers) are read during the call only.
+ * Errors: those of the calls it makes, checked for every block before the
+ * first launch (M2_EINVAL for a NULL pointer or an unknown kind, M2_ESHAPE
+ * for sizes the kernels do not take, M2_EALIGN, M2_EWORKSPACE). */
+m2_status mamba2_lm_step(const m2_lm* m, int n_sessions, void* hidden, const int32_t* lengths, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* T positions for S sessions at once, continuing from the caches (the
+ * full-history recompute when the caches start empty): hidden [S, T, hidden]
+ * bf16 in/out as mamba2_lm_step per position; the Mamba blocks run the
+ * chunked scan (mamba2_conv_scan_strided, `chunk`) over the T positions, the
+ * attention blocks the T positions in order (position t of session s at
+ * slot lengths[s] + t). Afterwards the caches are those after the last
+ * position; the caller advances lengths by T. Errors as mamba2_lm_step. */
+m2_status mamba2_lm_prefill(const m2_lm* m, int n_sessions, int T, void* hidden, const int32_t* lengths, int chunk,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* Static description of a status code. */
 const char* mamba2_status_string(m2_status s);

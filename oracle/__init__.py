@@ -67,6 +67,7 @@ def _load():
             lib.m2o_mixer_scan.argtypes = [ctypes.POINTER(_Dims)] + [dp] * 14 + [ip] * 4
             lib.m2o_mixer_step.argtypes = [ctypes.POINTER(_Dims), ip] + [dp] * 12 + [ip]
             lib.m2o_gated_norm.argtypes = [ip, ip, ip, dp, dp, dp, ctypes.c_double, dp]
+            lib.m2o_rmsnorm.argtypes = [ip, ip, dp, dp, ctypes.c_double, dp]
             lib.m2o_qlinear.argtypes = [ip, ip, ip, ip, ctypes.POINTER(ctypes.c_uint32), dp, dp, dp, dp]
             lib.m2o_attn_decode.argtypes = [ip] * 5 + [ctypes.POINTER(ctypes.c_int)] + [dp] * 5 + \
                 [ctypes.c_double, dp]
@@ -270,3 +271,20 @@ def attn_decode(q, k_new, v_new, k_cache, v_cache, lengths, scale: float) -> np.
                                  float(scale), _ptr(out))
     _check(rc, "attn_decode")
     return out
+
+
+def rmsnorm(x, weight, eps: float = 1e-5) -> np.ndarray:
+    """RMSNorm over the last axis: weight * x / sqrt(mean(x^2) + eps), fp64."""
+    x = _f64(x)
+    width = x.shape[-1]
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    out = np.empty_like(x)
+    rc = _load().m2o_rmsnorm(rows, width, _ptr(x), _ptr(_f64(weight)), float(eps), _ptr(out))
+    _check(rc, "rmsnorm")
+    return out
+
+
+def linear(x, w) -> np.ndarray:
+    """Dense linear layer without bias, y = x W^T (W [out, in]), fp64: a
+    library matrix product on the exact values."""
+    return _f64(x) @ _f64(w).T

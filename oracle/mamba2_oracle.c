@@ -393,6 +393,9 @@ int m2o_qlinear(int rows, int in, int out, int group, const uint32_t* wq, const 
     const int ngroups = in / group;
     for (long r = 0; r < rows; ++r)
         for (int o = 0; o < out; ++o) y[r * out + o] = 0.0;
+    /* outputs are independent: split them over threads (each y[.][o] is
+     * summed by one thread, in input order) */
+#pragma omp parallel for schedule(static)
     for (int o = 0; o < out; ++o) {
         for (int i = 0; i < in; ++i) {
             const uint32_t word = wq[(long)o * (in / 8) + i / 8];
@@ -465,5 +468,21 @@ int m2o_attn_decode(int S, int Hq, int Hkv, int D, int Tmax, const int* len, con
         }
     }
     free(a);
+    return M2O_OK;
+}
+
+/* RMSNorm of each row, the pre-norm of every block of the hybrid model
+ * (VoiceChat issue, section config.json / text_config: layer_norm_epsilon
+ * 1e-5):
+ *     out = weight * x / sqrt(mean over the row of x^2 + eps)
+ * x, out [rows, width]; weight [width]. */
+int m2o_rmsnorm(int rows, int width, const double* x, const double* weight, double eps, double* out) {
+    if (rows < 0 || width <= 0 || !x || !weight || !out || !(eps >= 0.0)) return M2O_EINVAL;
+    for (long r = 0; r < rows; ++r) {
+        double ss = 0.0;
+        for (int k = 0; k < width; ++k) ss += x[r * width + k] * x[r * width + k];
+        const double inv = 1.0 / sqrt(ss / width + eps);
+        for (int k = 0; k < width; ++k) out[r * width + k] = weight[k] * x[r * width + k] * inv;
+    }
     return M2O_OK;
 }

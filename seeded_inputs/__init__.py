@@ -44,6 +44,15 @@ __all__ = [
     "conv_state_inputs",
     "ssm_state_inputs",
     "norm_inputs",
+    "qlinear_inputs",
+    "attn_inputs",
+    "device_mixer_inputs",
+    "LMConfig",
+    "REAL_LM",
+    "TINY_LM",
+    "lm_weights",
+    "lm_hidden",
+    "device_lm_weights",
 ]
 
 
@@ -256,4 +265,112 @@ def attn_inputs(seed: int, S: int, Hq: int, Hkv: int, D: int, Tmax: int, lengths
         raise ValueError(f"act must be 'bf16' or 'f32', got {act!r}")
     out["lengths"] = np.ascontiguousarray(lengths, dtype=np.int32)
     out["act"] = act
+    return out
+
+
+# ------------------------------------------------------- hybrid language model
+@dataclass(frozen=True)
+class LMConfig:
+    """The blocks of the hybrid language model that the library runs: the
+    'M' (Mamba) and '*' (attention) entries of the layer pattern, in order."""
+
+    hidden: int
+    mixer: Dims
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    kinds: str
+    eps: float = 1e-5
+
+
+# Nemotron-H (VoiceChat issue, section config.json / text_config): hidden
+# 4480, the 27 'M' and 4 '*' entries of hybrid_override_pattern, attention
+# 40 / 8 heads of 128.
+REAL_LM = LMConfig(4480, REAL_SHAPE, 40, 8, 128, "".join(c for c in _PATTERN if c != "-"))
+# A small model of the same structure for brute-force and long-sequence checks.
+TINY_LM = LMConfig(256, Dims(H=8, P=16, N=16, G=2), 4, 2, 128, "MM*M*M")
+
+
+def _qweights(rng, n_out: int, n_in: int, group: int = 64):
+    """4-bit affine group-quantized weights drawn as qlinear_inputs draws them."""
+    wq = rng.integers(0, 2**32, size=(n_out, n_in // 8), dtype=np.uint64).astype(np.uint32)
+    ng = n_in // group
+    scales = rng.uniform(0.5, 1.5, size=(n_out, ng)) / (4.0 * np.sqrt(n_in))
+    biases = -7.5 * scales * rng.uniform(0.8, 1.2, size=(n_out, ng))
+    return wq, f32_to_bf16_bits(scales.astype(np.float32)), f32_to_bf16_bits(biases.astype(np.float32))
+
+
+def lm_weights(seed: int, cfg: LMConfig) -> list:
+    """Synthetic weights of every block (no checkpoint is involved), one dict
+    per block: norm weights ~ 1 + N(0, 0.1) fp32; 4-bit in_proj [2HP+2GN+H,
+    hidden] and out_proj [hidden, HP] drawn as qlinear_inputs draws them; the
+    mixer parameters of mixer_params; bf16 q|k|v [(Hq+2Hkv)D, hidden] and
+    output [hidden, Hq D] projections ~ N(0, 1/in)."""
+    d = cfg.mixer
+    W = 2 * d.H * d.P + 2 * d.G * d.N + d.H
+    out = []
+    for i, kind in enumerate(cfg.kinds):
+        rng = np.random.default_rng([seed, 0x5EED, 8, i])
+        L = {"norm_w": (1.0 + 0.1 * rng.standard_normal(cfg.hidden)).astype(np.float32)}
+        if kind == "M":
+            L["in_wq"], L["in_scales"], L["in_biases"] = _qweights(rng, W, cfg.hidden)
+            L.update(mixer_params(seed * 131 + i, d))
+            L["gnorm_w"] = (1.0 + 0.1 * rng.standard_normal(d.H * d.P)).astype(np.float32)
+            L["out_wq"], L["out_scales"], L["out_biases"] = _qweights(rng, cfg.hidden, d.H * d.P)
+        else:
+            nq = (cfg.n_heads + 2 * cfg.n_kv_heads) * cfg.head_dim
+            ao = cfg.n_heads * cfg.head_dim
+            L["wqkv"] = f32_to_bf16_bits(rng.standard_normal((nq, cfg.hidden), dtype=np.float32) / np.sqrt(cfg.hidden))
+            L["wo"] = f32_to_bf16_bits(rng.standard_normal((cfg.hidden, ao), dtype=np.float32) / np.sqrt(ao))
+        out.append(L)
+    return out
+
+
+def lm_hidden(seed: int, cfg: LMConfig, S: int, T: int) -> np.ndarray:
+    """Inputs of T positions of S sessions (the fused embeddings): [S, T,
+    hidden] ~ N(0, 1) as bf16 bit patterns."""
+    rng = np.random.default_rng([seed, 0x5EED, 9])
+    return f32_to_bf16_bits(rng.standard_normal((S, T, cfg.hidden), dtype=np.float32))
+
+
+def device_lm_weights(seed: int, cfg: LMConfig, device) -> list:
+    """lm_weights' distributions drawn on a device with torch's generator, for
+    the full-size model (1.5 GB of 4-bit and bf16 weights): torch tensors with
+    the same layouts and dtypes (bf16 fields as torch.bfloat16, packed 4-bit
+    words as int32)."""
+    import torch
+    d = cfg.mixer
+    W = 2 * d.H * d.P + 2 * d.G * d.N + d.H
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + 29)
+
+    def uni(shape, lo, hi):
+        return torch.rand(shape, generator=g, device=device, dtype=torch.float32) * (hi - lo) + lo
+
+    def qw(n_out, n_in):
+        wq = torch.randint(-2**31, 2**31 - 1, (n_out, n_in // 8), generator=g, device=device, dtype=torch.int32)
+        sc = uni((n_out, n_in // 64), 0.5, 1.5) / (4.0 * float(np.sqrt(n_in)))
+        bi = -7.5 * sc * uni((n_out, n_in // 64), 0.8, 1.2)
+        return wq, sc.to(torch.bfloat16), bi.to(torch.bfloat16)
+
+    out = []
+    for i, kind in enumerate(cfg.kinds):
+        L = {"norm_w": 1.0 + 0.1 * torch.randn(cfg.hidden, generator=g, device=device)}
+        if kind == "M":
+            L["in_wq"], L["in_scales"], L["in_biases"] = qw(W, cfg.hidden)
+            dt_target = torch.exp(uni((d.H,), float(np.log(1e-3)), float(np.log(0.1))).double())
+            L["dt_bias"] = torch.log(torch.expm1(dt_target)).float()
+            L["A_log"] = torch.log(uni((d.H,), 1.0, 16.0))
+            L["D"] = torch.randn(d.H, generator=g, device=device)
+            L["conv_w"] = uni((d.CH, d.K), -0.5, 0.5).contiguous()
+            L["conv_b"] = uni((d.CH,), -0.5, 0.5)
+            L["gnorm_w"] = 1.0 + 0.1 * torch.randn(d.H * d.P, generator=g, device=device)
+            L["out_wq"], L["out_scales"], L["out_biases"] = qw(cfg.hidden, d.H * d.P)
+        else:
+            nq = (cfg.n_heads + 2 * cfg.n_kv_heads) * cfg.head_dim
+            ao = cfg.n_heads * cfg.head_dim
+            L["wqkv"] = (torch.randn((nq, cfg.hidden), generator=g, device=device) / float(np.sqrt(cfg.hidden))
+                         ).to(torch.bfloat16)
+            L["wo"] = (torch.randn((cfg.hidden, ao), generator=g, device=device) / float(np.sqrt(ao))).to(torch.bfloat16)
+        out.append(L)
     return out

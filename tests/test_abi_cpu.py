@@ -168,3 +168,17 @@ def test_attn_decode_validation_without_gpu(m2):
     assert m2.mamba2_attn_decode_workspace_bytes(64, 40, 8, 128, 750) == 64 * 8 * 6 * 5 * 130 * 4
     assert call(wsb=need - 1) == 6
     assert m2.mamba2_attn_decode_workspace_bytes(2, 40, 8, 64, 100) == 0
+
+
+def test_noalloc_step_validation_without_gpu(m2):
+    """mamba2_step_noalloc checks its arguments as mamba2_step does, before the
+    size of its scratch and before any device set-up: a NULL pointer is
+    M2_EINVAL and a misaligned one M2_EALIGN even with no GPU, and a request
+    beyond the scratch is M2_EWORKSPACE."""
+    d = m2.dims(0, 0, 128, 80, 128, 8, 4, "bf16")
+    p = _fake_ptrs(12)
+    assert m2.mamba2_step_noalloc(d, 2, None, *p[1:], stream=0, check=False) == 1
+    assert m2.mamba2_step_noalloc(d, -1, *p, stream=0, check=False) == 1
+    assert m2.mamba2_step_noalloc(d, 2, p[0] + 8, *p[1:], stream=0, check=False) == 3
+    assert m2.mamba2_step_noalloc(m2.dims(0, 0, 4, 16, 24, 1, 4, "f32"), 2, *p, stream=0, check=False) == 2
+    assert m2.mamba2_step_noalloc(d, 22, *p, stream=0, check=False) == 6

@@ -581,3 +581,122 @@ def test_attn_appends_and_touches_nothing_else():
     np.testing.assert_array_equal(c["v_cache"], v0)
     with pytest.raises(RuntimeError):
         oracle.attn_decode(c["q"], c["k_new"], c["v_new"], c["k_cache"], c["v_cache"], [0, 2, 6], 0.35)
+
+
+# ------------------------------------------------ hybrid model blocks (NEXT-4)
+def test_rmsnorm_is_torch_rms_norm():
+    import oracle
+    rng = np.random.default_rng(40)
+    x = rng.standard_normal((5, 96))
+    w = 1 + 0.1 * rng.standard_normal(96)
+    ref = torch.nn.functional.rms_norm(torch.tensor(x), (96,), torch.tensor(w), eps=1e-5).numpy()
+    assert rel(oracle.rmsnorm(x, w, 1e-5), ref) < 1e-14
+
+
+def test_rmsnorm_worked_case():
+    """x = (3, 4): mean of squares 12.5, so x / sqrt(12.5) = (0.8485.., 1.1313..)."""
+    import oracle
+    out = oracle.rmsnorm(np.array([[3.0, 4.0]]), np.array([1.0, 2.0]), 0.0)
+    np.testing.assert_allclose(out, [[3 / np.sqrt(12.5), 8 / np.sqrt(12.5)]], rtol=1e-15)
+
+
+def _tiny_lm(S=2, max_len=16, seed=41):
+    from oracle.lm import LMOracle
+    from seeded_inputs import TINY_LM, lm_weights
+    return LMOracle(TINY_LM, lm_weights(seed, TINY_LM), S, max_len)
+
+
+def test_lm_stepping_equals_recompute():
+    """The cached position stepped T times == the full-history recompute of
+    the T positions (scan form of every Mamba block, attention over the
+    positions in order): the model-level form of the Offline-timeline
+    statement that both modes give the same tokens."""
+    from seeded_inputs import TINY_LM, lm_hidden
+    S, T = 2, 7
+    H = lm_hidden(42, TINY_LM, S, T)
+    a, b = _tiny_lm(S), _tiny_lm(S)
+    stepped = np.stack([a.step(H[:, t]) for t in range(T)], axis=1)
+    recomputed = b.prefill(H)
+    assert rel(stepped, recomputed) < 1e-12
+    for i in a.ssm:
+        assert rel(a.ssm[i], b.ssm[i]) < 1e-12
+        np.testing.assert_array_equal(a.conv[i], b.conv[i])
+    for i in a.kc:
+        np.testing.assert_array_equal(a.kc[i], b.kc[i])
+    np.testing.assert_array_equal(a.lengths, b.lengths)
+
+
+def test_lm_recompute_continues_from_its_caches():
+    """Prefill of T1 positions, then of T2 more from the caches it left ==
+    prefill of all T1 + T2 positions at once."""
+    from seeded_inputs import TINY_LM, lm_hidden
+    S, T1, T2 = 2, 3, 5
+    H = lm_hidden(43, TINY_LM, S, T1 + T2)
+    a, b = _tiny_lm(S), _tiny_lm(S)
+    two = np.concatenate([a.prefill(H[:, :T1]), a.prefill(H[:, T1:])], axis=1)
+    assert rel(two, b.prefill(H)) < 1e-12
+
+
+def test_lm_blocks_with_zero_output_weights_pass_h_through():
+    """With out_proj and Wo zero every block adds exactly zero: the residual
+    stream leaves the last block as it entered (bf16 values stay exact)."""
+    from seeded_inputs import TINY_LM, lm_hidden
+    from oracle.lm import rb
+    lm = _tiny_lm(2)
+    for L in lm.w:
+        if "out_scales" in L:
+            L["out_scales"] = np.zeros_like(L["out_scales"])
+            L["out_biases"] = np.zeros_like(L["out_biases"])
+        else:
+            L["wo"] = np.zeros_like(L["wo"])
+    H = lm_hidden(44, TINY_LM, 2, 1)
+    h0 = rb(as_f64(H[:, 0], "bf16"))
+    np.testing.assert_array_equal(lm.step(H[:, 0]), h0)
+    assert np.any(lm.ssm[0] != 0)  # the blocks did run
+
+
+def test_lm_first_position_attention_returns_its_value():
+    """At the first position each attention block attends only to the new
+    key, so its output is the new value: o = v exactly (softmax of one
+    score), which pins the q|k|v split of the projection."""
+    from seeded_inputs import TINY_LM, lm_hidden
+    lm = _tiny_lm(1)
+    i = TINY_LM.kinds.index("*")
+    H = lm_hidden(45, TINY_LM, 1, 1)
+    h = as_f64(H[:, 0], "bf16")
+    # run the blocks before the first attention block, then its projections
+    for j in range(i):
+        L = lm.w[j]
+        proj = lm._mamba_in(L, h)
+        z, x, B, C, dt = lm._split(proj)
+        d = TINY_LM.mixer
+        frame = dict(x=x.reshape(1, d.H, d.P), B=B.reshape(1, d.G, d.N), C=C.reshape(1, d.G, d.N), dt_raw=dt,
+                     act="f32")
+        from oracle import mixer_step
+        y = np.asarray(mixer_step(d, frame, L, lm.ssm[j], lm.conv[j])).reshape(1, -1)
+        from oracle.lm import rb
+        h = lm._mamba_out(L, h, rb(y), z)
+    q, k, v = lm._qkv(lm.w[i], h)
+    o = lm._attend(i, q, k, v, 0)
+    R = TINY_LM.n_heads // TINY_LM.n_kv_heads
+    np.testing.assert_array_equal(o.reshape(TINY_LM.n_heads, -1),
+                                  np.repeat(v.reshape(TINY_LM.n_kv_heads, -1), R, axis=0))
+
+
+def test_lm_drift_gate_catches_a_missing_block():
+    """The end-to-end gate has the power it claims: the oracle's position
+    with one block left out lies beyond it."""
+    from oracle.lm import LMOracle
+    from seeded_inputs import TINY_LM, LMConfig, lm_hidden, lm_weights
+    from m2_testlib import BF16_U
+    cfg = TINY_LM
+    w = lm_weights(562, cfg)
+    H = lm_hidden(563, cfg, 2, 1)
+    full = LMOracle(cfg, w, 2, 4).step(H[:, 0])
+    for drop in range(len(cfg.kinds)):
+        keep = [i for i in range(len(cfg.kinds)) if i != drop]
+        sub = LMConfig(cfg.hidden, cfg.mixer, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim,
+                       "".join(cfg.kinds[i] for i in keep), cfg.eps)
+        part = LMOracle(sub, [w[i] for i in keep], 2, 4).step(H[:, 0])
+        err = np.linalg.norm(part - full) / np.linalg.norm(full)
+        assert err > 2.0 * BF16_U * np.sqrt(len(cfg.kinds)), drop
