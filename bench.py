@@ -49,21 +49,31 @@ METRIC = "Mamba2 scan tokens/s and per-frame step µs; % of HBM / bf16 MMA roofl
 WORKLOAD = ("Nemotron-H Mamba2 mixer, real shape H=128 P=80 N=128 G=8 K=4, batch 1, T=300 chunked scan "
             "(chunk 128) + 1 cached step, bf16 activations / fp32 state, 27 layers cycled")
 
-# Algorithmic work (per unit, stated in the design doc):
+# Algorithmic work per unit:
 #   scan bytes per token: x|B|C in 24,576 + dt 256 + y out 20,480 = 45,312 B
 #   plus the final fp32 state (H*P*N*4 = 5,242,880 B) and conv tail (3*12288*2) per sequence.
-#   scan MMA flops per token (dense, chunk 128): C.B^T 2*Q*N*G + M.x 2*Q*P*H + state 2*N*P*H
-#   + C.h 2*N*P*H = 8,126,464.
+#   scan MMA flops per token at chunk Q, counting the causal (lower-triangular)
+#   half of the two Q x Q products: C.B^T Q*N*G + M.x Q*P*H + chunk state
+#   2*N*P*H + C.h 2*N*P*H = 6,684,672 at Q = 128 (5,963,776 at Q = 64).
 #   step bytes per session: 2 x 5,242,880 state + 2 x 73,728 conv tail + 24,832 in + 20,480 out.
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one SSD-kernel
-# launch of this workload, from the ncu capture summarised in
-# profiles/scan_ssd_kernel_b1_T300.md. It describes one version of the kernel
-# source; for any other version the traffic is reported as unknown (null).
+# launch of this workload, from an ncu capture of the kernel. It describes one
+# version of the kernel source; for any other version the traffic is reported
+# as unknown (null).
 SSD_TRAFFIC = {"bytes": 8884224, "m2_scan_cu_sha1": "9e2a4ebb20f9330387da1e26c7400001fcaf45ce"}
 SCAN_BYTES_PER_TOKEN = 45312
 STATE_BYTES = 128 * 80 * 128 * 4
 TAIL_BYTES = 3 * 12288 * 2
-SCAN_FLOPS_PER_TOKEN = 2 * CHUNK * 128 * 8 + 3 * (2 * 128 * 80 * 128)
+
+
+def scan_flops_per_token(q):
+    """Algorithmic MMA flops per token of the chunked scan at chunk length q
+    (causal halves of the two q x q products; the chunk state and C.h in full)."""
+    H, P, N, G = 128, 80, 128, 8
+    return q * N * G + q * P * H + 4 * N * P * H
+
+
+SCAN_FLOPS_PER_TOKEN = scan_flops_per_token(CHUNK)
 STEP_BYTES_PER_SESSION = 2 * STATE_BYTES + 2 * TAIL_BYTES + 24832 + 20480
 
 
@@ -377,6 +387,61 @@ def _sessions_step_args(m2, torch, dev, L, S):
             p["conv_b"], ssm, conv, y, ws)
 
 
+def lm_position_bytes(cfg, S, cached):
+    """Algorithmic bytes of one cached position: every weight read once
+    (4-bit fields with their bf16 scales and biases; bf16 attention
+    projections), each Mamba block's fp32 state and conv tail read and
+    written, each attention block's cached keys and values read and the new
+    ones written, the residual stream read and written per block."""
+    d = cfg.mixer
+    HP, GN = d.H * d.P, d.G * d.N
+    W = 2 * HP + 2 * GN + d.H
+    q4 = lambda o, i: o * i // 2 + 2 * o * (i // 64) * 2  # noqa: E731
+    m = q4(W, cfg.hidden) + q4(cfg.hidden, HP) + S * (2 * HP * d.N * 4 + 2 * 3 * d.CH * 2)
+    kv = cfg.n_kv_heads * cfg.head_dim * 2
+    a = ((cfg.n_heads + 2 * cfg.n_kv_heads) * cfg.head_dim * cfg.hidden + cfg.hidden * cfg.n_heads * cfg.head_dim) * 2
+    a += S * (2 * kv * cached + 2 * kv)
+    nm, na = cfg.kinds.count("M"), cfg.kinds.count("*")
+    return nm * m + na * a + len(cfg.kinds) * S * cfg.hidden * 2 * 2
+
+
+def lm_position_leg(m2, torch, dev, stream, peaks):
+    from seeded_inputs import REAL_LM, device_lm_weights
+    cfg, S, cached, max_len = REAL_LM, 1, 750, 1024
+    d = cfg.mixer
+    wdev = device_lm_weights(7, cfg, dev)
+    layers = []
+    for i, kind in enumerate(cfg.kinds):
+        L = dict(wdev[i])
+        if kind == "M":
+            L["ssm_state"] = torch.zeros((S, d.H, d.P, d.N), device=dev)
+            L["conv_state"] = torch.zeros((S, d.K - 1, d.CH), dtype=torch.bfloat16, device=dev)
+        else:
+            shape = (S, cfg.n_kv_heads, max_len, cfg.head_dim)
+            L["k_cache"] = torch.randn(shape, device=dev).to(torch.bfloat16)
+            L["v_cache"] = torch.randn(shape, device=dev).to(torch.bfloat16)
+        layers.append(L)
+    model = m2.lm_model(cfg.kinds, layers, cfg.hidden, m2.dims(0, 0, d.H, d.P, d.N, d.G, d.K, "bf16"), cfg.n_heads,
+                        cfg.n_kv_heads, cfg.head_dim, max_len, cfg.eps)
+    ws = torch.empty(m2.mamba2_lm_workspace_bytes(model, S, 1, 1), dtype=torch.uint8, device=dev)
+    lens = torch.full((S,), cached, dtype=torch.int32, device=dev)
+    h = torch.randn((S, cfg.hidden), device=dev).to(torch.bfloat16)
+    torch.cuda.synchronize()
+
+    def one():
+        m2.mamba2_lm_step(model, S, h, lens, ws, stream=stream)
+
+    us = _time_graph(torch, stream, one, reps=20)
+    nbytes = lm_position_bytes(cfg, S, cached)
+    out = {"sessions": S, "blocks": cfg.kinds, "cached_positions": cached, "us_per_position": us,
+           "bytes_per_position": nbytes, "achieved_gbs": nbytes / (us * 1e-6) / 1e9,
+           "frac_hbm": nbytes / (us * 1e-6) / 1e9 / peaks["hbm"],
+           "kernels_per_position": 4 * cfg.kinds.count("M") + 4 * cfg.kinds.count("*")}
+    del wdev, layers, model, ws
+    torch.cuda.synchronize()
+    return out
+
+
 def run_gpu(args, world, rank, local):
     import torch
     from full_duplex_speech_gb300 import build as m2build
@@ -504,6 +569,31 @@ def run_gpu(args, world, rank, local):
               "achieved_gbs": 64 * STEP_BYTES_PER_SESSION / (s64_us * 1e-6) / 1e9}
     step64["frac_hbm"] = step64["achieved_gbs"] / peaks["hbm"]
     del s64
+    torch.cuda.synchronize()
+
+    # the whole scan (both kernels) of the real-scan workload at chunk 64 and
+    # 128, 27 layers cycled in a graph; tensor figures from each chunk's
+    # algorithmic flops
+    chunk_sweep = {}
+    torch.cuda.nvtx.range_push("chunk_sweep")
+    for q in (64, 128):
+        qws = [torch.empty(m2.mamba2_scan_workspace_bytes(L.dims, q), dtype=torch.uint8, device=dev)
+               for L in layers]
+        torch.cuda.synchronize()
+
+        def q_scans():
+            for L, w in zip(layers, qws):
+                a = list(L.scan_args())
+                a[10], a[16] = q, w
+                m2.mamba2_conv_scan(*a, stream=stream)
+
+        q_us = _time_graph(torch, stream, q_scans, reps=20) / N_LAYERS
+        q_tfs = scan_flops_per_token(q) * T_FRAMES / (q_us * 1e-6) / 1e12
+        chunk_sweep[str(q)] = {"us_per_scan": q_us, "tokens_per_s": T_FRAMES / (q_us * 1e-6),
+                               "algorithmic_tflops": q_tfs, "frac_bf16": q_tfs / peaks["bf16"],
+                               "note": "whole scan (B/C prologue + SSD kernel); flops of the SSD contractions"}
+        del qws
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
 
     # the gated output norm over the T=300 rows of a scan's y (8 buffer sets
@@ -640,6 +730,12 @@ def run_gpu(args, world, rank, local):
     del pf, py, pfs, pfc, pws
     torch.cuda.synchronize()
 
+    # one cached position of the hybrid model (27 Mamba + 4 attention blocks
+    # of Nemotron-H at full size, synthetic weights, one session with 750
+    # positions in its KV caches): mamba2_lm_step replayed from a CUDA graph;
+    # the weights (2.7 GB) exceed L2, so every replay streams them again
+    lm = lm_position_leg(m2, torch, dev, stream, peaks)
+
     # End to end through the C ABI with host buffers: every step copies its
     # inputs in from pinned host memory (one copy) and its results out (one
     # copy), around the public calls (mamba2_conv_scan, mamba2_step). Three
@@ -698,10 +794,15 @@ def run_gpu(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         v, info = oracle_tokens_per_s(args.cpu_seconds, nthreads)
+        v1, info1 = oracle_tokens_per_s(args.cpu_seconds / 2, 1, heads_cap=4)
         cpu = {"value": v, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
                "sample": (f"fp64 oracle, one layer: 301-frame recurrence (300 prefill + 1 cached) for "
                           f"{info['heads']} of 128 heads, {info['reps']} reps in {info['seconds']:.1f} s, "
-                          f"scaled by 128/{info['heads']}")}
+                          f"scaled by 128/{info['heads']}"),
+               "single_thread": {"value": v1, "unit": "tokens/s", "cores": 1,
+                                 "sample": (f"the same recurrence on one thread for {info1['heads']} heads, "
+                                            f"{info1['reps']} reps in {info1['seconds']:.1f} s, scaled by "
+                                            f"128/{info1['heads']}")}}
 
     if rank == 0:
         line = {
@@ -716,11 +817,18 @@ def run_gpu(args, world, rank, local):
                          "frac": ssd_gbs / peaks["hbm"],
                          "traffic": args.ssd_traffic if args.ssd_traffic is not None else ssd_traffic_for_current_source(),
                          "algorithmic_bytes_per_launch": ssd_bytes, "avg_launch_ms": ssd_avg,
+                         "byte_counts": ("achieved = algorithmic_bytes_per_launch / avg_launch_ms; traffic = "
+                                         "measured DRAM bytes per launch (ncu), lower than the algorithmic "
+                                         "bytes because y and the final state are still in L2 when the "
+                                         "kernel ends"),
+                         "tensor_fraction": "roofline_tensor (the scan's own target is a bf16 tensor fraction)",
                          "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
                          "timing": timing_src},
             "roofline_tensor": {"kernel": "scan_ssd_kernel", "achieved": ssd_tfs, "peak": peaks["bf16"],
                                 "unit": "TFLOP/s", "frac": ssd_tfs / peaks["bf16"],
-                                "algorithmic_flops_per_launch": ssd_flops},
+                                "algorithmic_flops_per_launch": ssd_flops,
+                                "flops": "causal halves of the two chunk x chunk products, chunk 128"},
+            "scan_chunk_sweep_T300": chunk_sweep,
             "step": {"us_per_layer_call_in_bench_step": step_avg * 1e3, "achieved_gbs": step_gbs,
                      "frac_hbm": step_gbs / peaks["hbm"], "bytes_per_call": STEP_BYTES_PER_SESSION,
                      "sessions": 1},
@@ -730,6 +838,7 @@ def run_gpu(args, world, rank, local):
             "qlinear_4bit_g64": qlinear,
             "attn_decode": attn,
             "prefill_b4_T4096": prefill,
+            "lm_position_b1": lm,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": 4 * K,
