@@ -195,24 +195,52 @@ __device__ void write_tail(const ScanArgs& a, int b, long c) {
 }
 
 // ----------------------------------------------------------------- kernel 2
-// Eight compute warps (two per TMEM lane quarter, each taking half of the P
-// columns) and one control warp whose elected thread issues every TMA copy
-// and tcgen05 instruction. The issuing thread stalls while the tensor cores
-// work through its MMAs, so it is kept out of the CUDA-core phases.
-constexpr int kComputeThreads = 256;
+// kComputeWarps compute warps and one control warp whose elected thread
+// issues every TMA copy and tcgen05 instruction. The issuing thread stalls
+// while the tensor cores work through its MMAs, so it is kept out of the
+// CUDA-core phases. Compute warp w works on TMEM lane quarter w % 4 (rows
+// 32(w % 4) .. +31 of a chunk, or of the state's n) and on column part w / 4:
+// the P columns, in units of 8, are split over the parts as evenly as they
+// go, and the 128 columns j of the decay mask go to the parts with fewer P
+// columns (to every part alike when the units split evenly).
+constexpr int kComputeWarps = 16;
+constexpr int kParts = kComputeWarps / 4;
+constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kSsdThreads = kComputeThreads + 32;
 constexpr int kCtrl = kComputeThreads;  // the control thread
+constexpr int kDtPart = kParts - 1;     // the column part that also computes dt and S
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kRawRows = kTR + 3;  // pre-conv rows of one chunk plus the 3-frame halo
+static_assert(kComputeWarps == 8 || kComputeWarps == 16, "two or four column parts");
 // TMEM columns
 // M, the masked G in bf16, is the A operand of Y_diag straight from TMEM:
-// row i on lane i, two columns j per 32-bit TMEM column. Each half of the
-// compute warps writes its 64 columns j of M over the first 32 of the 64 G
-// columns it has just read (so M for j = 64h + k sits at column 64h + k/2).
-// Y_off is double-buffered by chunk parity: a chunk's Y_off MMAs run while
-// the previous chunk's y is still being read.
+// row i on lane i, two columns j per 32-bit TMEM column. A part writes the M
+// of its mask columns over the first half of the G columns it has just read
+// (SsdParts::m_col). Y_off is double-buffered by chunk parity: a chunk's
+// Y_off MMAs run while the previous chunk's y is still being read.
 constexpr uint32_t kColG = 0, kColState = 128, kColYd = 224, kColYo0 = 320, kColYo1 = 416, kTmemCols = 512;
 static_assert(kColYo1 + 80 <= kTmemCols, "accumulators of up to 80 columns fit the allocation");
+
+// How the column work of one head is split over the column parts.
+template <int P>
+struct SsdParts {
+    static constexpr int U = P / 8;                          // 8-column units of P
+    static constexpr int kBase = U / kParts, kRem = U % kParts;
+    static constexpr int kMaxUnits = kBase + (kRem ? 1 : 0);
+    // parts below kRem carry one unit more; the mask then goes to the others
+    static constexpr int kMaskParts = kRem ? kParts - kRem : kParts;
+    static constexpr int kMaskSteps = 8 / kMaskParts;        // K-steps of 16 mask columns per mask part
+    static_assert(kMaskSteps * kMaskParts == 8, "the mask's 8 K-steps split evenly");
+    __device__ static int units(int part) { return kBase + (part < kRem ? 1 : 0); }
+    __device__ static int first_unit(int part) { return part * kBase + min(part, kRem); }
+    __device__ static int mask_steps(int part) { return (kRem && part < kRem) ? 0 : kMaskSteps; }
+    __device__ static int first_mask_step(int part) { return (kRem ? part - kRem : part) * kMaskSteps; }
+    // TMEM column (from kColG) of the M of K-step ks: the part that owns ks
+    // writes 8 columns per step from the start of the G columns it read
+    __host__ __device__ static constexpr uint32_t m_col(int ks) {
+        return (uint32_t)((ks / kMaskSteps) * kMaskSteps * 16 + (ks % kMaskSteps) * 8);
+    }
+};
 
 template <typename TA, int P>
 struct SsdSmem {
@@ -234,8 +262,8 @@ struct SsdSmem {
     static constexpr uint32_t kS = kRaw + kRawRows * kRowBytes;  // float S[128]
     static constexpr uint32_t kDt = kS + 512;             // float dt[128]
     static constexpr uint32_t kTj = kDt + 512;            // float exp(S_j1 - S_j) dt_j, j1 = j | 7 [128]
-    static constexpr uint32_t kWsum = kTj + 512;          // float warp sums[8]
-    static constexpr uint32_t kCw = kWsum + 64;           // float conv_w[P][4]
+    static constexpr uint32_t kWsum = kTj + 512;          // float warp sums[4]
+    static constexpr uint32_t kCw = kWsum + 64;           // float conv_w[4][P] (tap-major)
     static constexpr uint32_t kCb = kCw + P * 16;         // float conv_b[P]
     static constexpr uint32_t kBar = (kCb + P * 4 + 15) / 16 * 16;  // 9 mbarriers
     static constexpr uint32_t kTmem = kBar + 72;          // TMEM base address
@@ -249,6 +277,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
     return r;
 }
+__device__ __forceinline__ uint32_t pack2(float2 v) { return pack2(v.x, v.y); }
 
 // 2^x on the special-function unit (ex2.approx: relative error ~2^-22, ftz).
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -256,9 +285,80 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
+// 1/x on the special-function unit (rcp.approx, ftz: 0 for |x| above 2^126).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
 
-// Barrier among the eight compute warps only (the control warp never joins).
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Paired fp32 arithmetic: one instruction for two lanes of values, each
+// rounded exactly as its scalar counterpart.
+__device__ __forceinline__ uint64_t f2_bits(float2 v) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+    return r;
+}
+__device__ __forceinline__ float2 f2_of(uint64_t r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+    return f2_of(r);
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return f2_of(r);
+}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return f2_of(r);
+}
+__device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return f2_of(r);
+}
+__device__ __forceinline__ float2 f2_splat(float v) { return make_float2(v, v); }
+// a bf16 pair (low half first) as two fp32 values
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// SiLU(u) = u / (1 + 2^(-u log2 e)) on a pair, with the special-function
+// unit's exponential and reciprocal. Where the divisor is huge (u below about
+// -87) the reciprocal is 0, and so is the result (exactly: below 1e-36).
+__device__ __forceinline__ float2 silu2(float2 u) {
+    const float2 t = f2_mul(u, f2_splat(-kLog2e));
+    const float2 d = f2_add(make_float2(ex2_approx(t.x), ex2_approx(t.y)), f2_splat(1.f));
+    return f2_mul(u, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
+// Eight consecutive activations of one staged row as four fp32 pairs.
+template <typename TA>
+__device__ __forceinline__ void load8_pairs(const uint8_t* p, float2 (&v)[4]) {
+    if constexpr (sizeof(TA) == 2) {
+        const uint4 r = *reinterpret_cast<const uint4*>(p);
+        v[0] = bf2_to_f2(r.x);
+        v[1] = bf2_to_f2(r.y);
+        v[2] = bf2_to_f2(r.z);
+        v[3] = bf2_to_f2(r.w);
+    } else {
+        const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+        v[0] = make_float2(a.x, a.y);
+        v[1] = make_float2(a.z, a.w);
+        v[2] = make_float2(b.x, b.y);
+        v[3] = make_float2(b.z, b.w);
+    }
+}
+
+// Barrier among the compute warps only (the control warp never joins).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory"); }
 
 // Stages the pre-conv x rows of chunk c (frames c0-3 .. c0+kTR-1) of this head
 // into shared memory with one 3-D TMA box copy of [kRawRows frames x P
@@ -273,23 +373,30 @@ __device__ __forceinline__ void stage_raw_x(const CUtensorMap* tmx, uint8_t* raw
 }
 
 template <typename TA, int P>
-__global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, int nchunks,
+// Seventeen warps put five on one SM sub-partition, whose register file then
+// allows at most 96 registers a thread: the bound below (20 warps' worth) asks
+// the compiler for that.
+__global__ void __launch_bounds__(kComputeWarps == 16 ? 640 : kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, int nchunks,
                                                                   const __grid_constant__ CUtensorMap tmx) {
     using L = SsdSmem<TA, P>;
-    constexpr int PH = P / 2;   // columns handled by each half of the compute warps
-    constexpr int NQ = PH / 8;  // 8-column groups per half
+    using Parts = SsdParts<P>;
+    constexpr int NU = Parts::kMaxUnits;       // 8-column units of a part, at most
+    constexpr int NK = Parts::kMaskSteps;      // mask K-steps of a mask part
     constexpr uint32_t LBO_I = (P / 8) * 128;  // K-group stride of the interleaved tiles
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // offset from the shared array itself, so that the compiler keeps the shared address space
+    uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
 
     const Shape& s = a.s;
     const int h = blockIdx.x, b = blockIdx.y;
     const int g = h / (s.H / s.G);
     const int T = a.T, Q = a.chunk;
     const long HP = s.HP();
-    const int tid = threadIdx.x, row = tid & 127, half = (tid >> 7) & 1, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, row = tid & 127, part = tid >> 7, warp = tid >> 5, lane = tid & 31;
     const bool compute = tid < kComputeThreads;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int quarter = warp & 3;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int nu = compute ? Parts::units(part) : 0, u0 = Parts::first_unit(part);
 
     float* sS = reinterpret_cast<float*>(sm + L::kS);
     float* sDt = reinterpret_cast<float*>(sm + L::kDt);
@@ -302,10 +409,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     uint64_t* bar_b = bar_a + 1;                                   // B~ lo tile landed
     uint64_t* bar_x = bar_a + 2;                                   // pre-conv x rows landed
     uint64_t* bar_g = bar_a + 3;                                   // G done
-    uint64_t* bar_op0 = bar_a + 4;                                 // h_prev tile written (256 arrivals)
+    uint64_t* bar_op0 = bar_a + 4;                                 // h_prev tile written (all compute threads)
     uint64_t* bar_y = bar_a + 5;                                   // every MMA of the chunk done
-    uint64_t* bar_op1 = bar_a + 6;                                 // phase-1 operands written (256 arrivals)
-    uint64_t* bar_op2 = bar_a + 7;                                 // phase-2 operands written (256 arrivals)
+    uint64_t* bar_op1 = bar_a + 6;                                 // phase-1 operands written (all compute threads)
+    uint64_t* bar_op2 = bar_a + 7;                                 // phase-2 operands written (all compute threads)
     uint64_t* bar_end = bar_a + 8;                                 // MMAs of an abandoned chunk done
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::kTmem);
     volatile uint32_t* sFlag = reinterpret_cast<uint32_t*>(sm + L::kFlag);
@@ -362,11 +469,16 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     const float A_log_h = ldg_pinned_f32(a.A_log + h);
     const float Dh = ldg_pinned_f32(a.D + h);
     const float dtb = ldg_pinned_f32(a.dt_bias + h);
+    const bool dt_part = compute && part == kDtPart;
     ActRaw<TA> dt_raw_bits = 0;
-    if (compute && nchb > 0 && half == 0 && row < min(Q, Tb))
+    if (dt_part && nchb > 0 && row < min(Q, Tb))
         dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + row) * a.fdt + h);
     if (tid < P) {
-        reinterpret_cast<float4*>(sCw)[tid] = cw;
+        // tap-major, so that one 16-byte load gives a tap's weights of four channels
+        sCw[0 * P + tid] = cw.x;
+        sCw[1 * P + tid] = cw.y;
+        sCw[2 * P + tid] = cw.z;
+        sCw[3 * P + tid] = cw.w;
         sCb[tid] = cb;
     }
     const float A = -expf(A_log_h);
@@ -381,16 +493,33 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
 
     if (!compute) {
         // ================================================================ control
-        if (tid == kCtrl && nchb > 0) {
+        // The whole warp runs the loop (so that the descriptor arithmetic stays
+        // warp-uniform); one elected lane issues every copy and MMA.
+        if (nchb > 0) {
+            const bool leader = tc::elect_one();
             pdl_wait();  // the operand tiles are the prologue kernel's output
             const uint8_t* src = tiles_of(0);
-            tc::mbar_arrive_expect_tx(bar_a, 2 * kTileBytes);
-            tc::bulk_g2s(sm + L::kBh, src, kTileBytes, bar_a);
-            tc::bulk_g2s(sm + L::kC, src + 2 * kTileBytes, kTileBytes, bar_a);
-            tc::mbar_arrive_expect_tx(bar_b, kTileBytes);
-            tc::bulk_g2s(sm + L::kBl, src + kTileBytes, kTileBytes, bar_b);
-            const uint32_t sC = sbase + L::kC, sBh = sbase + L::kBh, sBl = sbase + L::kBl;
-            const uint32_t sX = sbase + L::kX, sWh = sbase + L::kWh, sWl = sbase + L::kWl, sH = sbase + L::kH;
+            if (leader) {
+                tc::mbar_arrive_expect_tx(bar_a, 2 * kTileBytes);
+                tc::bulk_g2s(sm + L::kBh, src, kTileBytes, bar_a);
+                tc::bulk_g2s(sm + L::kC, src + 2 * kTileBytes, kTileBytes, bar_a);
+                tc::mbar_arrive_expect_tx(bar_b, kTileBytes);
+                tc::bulk_g2s(sm + L::kBl, src + kTileBytes, kTileBytes, bar_b);
+            }
+            __syncwarp();
+            // Matrix descriptors of every operand at K-step 0; a K-step's
+            // descriptor adds its byte offset / 16 to the start-address field.
+            const uint64_t dCk = tc::sdesc(sbase + L::kC, 0, 1024, 2);    // C~, K-major (K = n)
+            const uint64_t dBk = tc::sdesc(sbase + L::kBh, 0, 1024, 2);   // B~ hi, K-major (K = n)
+            const uint64_t dBhm = tc::sdesc(sbase + L::kBh, kPanel, 1024, 2);  // B~ hi as B~^T, MN-major (K = j)
+            const uint64_t dBlm = tc::sdesc(sbase + L::kBl, kPanel, 1024, 2);  // B~ lo as B~^T
+            const uint64_t dH = tc::sdesc(sbase + L::kH, LBO_I, 128, 0);   // h_prev, MN-major interleave (K = n)
+            const uint64_t dWh = tc::sdesc(sbase + L::kWh, LBO_I, 128, 0);  // (w o x~) hi (K = j)
+            const uint64_t dWl = tc::sdesc(sbase + L::kWl, LBO_I, 128, 0);  // (w o x~) lo
+            const uint64_t dX = tc::sdesc(sbase + L::kX, LBO_I, 128, 0);    // x~ hi (K = j)
+            auto koff_k = [](int ks) { return (uint64_t)(((ks >> 2) * kPanel + (ks & 3) * 32) >> 4); };
+            auto koff_m = [](int ks) { return (uint64_t)((ks * 2048) >> 4); };
+            auto koff_i = [](int ks) { return (uint64_t)((ks * 2 * LBO_I) >> 4); };
             const uint32_t idG = tc::idesc_bf16(128, 128, 0, 0);
             const uint32_t idS = tc::idesc_bf16(128, P, 1, 1);
             const uint32_t idY = tc::idesc_bf16(128, P, 0, 1);
@@ -406,13 +535,13 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 const bool okt = wait_ok(bar_a, par, ERR_MBAR_TIMEOUT_LOAD);
                 if (okt) {
                     tc::tc_fence_after();
+                    if (leader) {
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
-                        tc::mma_bf16(tm + kColG, tc::sdesc(sC + koff, 0, 1024, 2), tc::sdesc(sBh + koff, 0, 1024, 2),
-                                     idG, ks > 0);
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_bf16(tm + kColG, dCk + koff_k(ks), dBk + koff_k(ks), idG, ks > 0);
+                        tc::mma_commit(bar_g);
                     }
-                    tc::mma_commit(bar_g);
+                    __syncwarp();
                 }
                 // Y_off = C~ h_prev^T as soon as the h_prev tile is written: it runs
                 // under the compute warps' conv (into the Y_off buffer of this
@@ -422,12 +551,12 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                 tc::tc_fence_after();
                 const uint32_t colYo = par ? kColYo1 : kColYo0;
                 if (ok0 && okt) {
+                    if (leader) {
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t koff = (ks >> 2) * kPanel + (ks & 3) * 32;
-                        tc::mma_bf16(tm + colYo, tc::sdesc(sC + koff, 0, 1024, 2),
-                                     tc::sdesc(sH + ks * 2 * LBO_I, LBO_I, 128, 0), idY, ks > 0);
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_bf16(tm + colYo, dCk + koff_k(ks), dH + koff_i(ks), idY, ks > 0);
                     }
+                    __syncwarp();
                 }
                 const bool ok1 = wait_ok(bar_op1, par, ERR_MBAR_TIMEOUT_MMA);
                 tc::tc_fence_after();
@@ -437,39 +566,52 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                     // fresh sequence's state is not in TMEM before its first chunk:
                     // that chunk's first product overwrites the accumulator.
                     const uint32_t acc0 = (c > 0 || a.init_ssm != nullptr) ? 1u : 0u;
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        const uint64_t dBh = tc::sdesc(sBh + ks * 2048, kPanel, 1024, 2);
-                        const uint64_t dWh = tc::sdesc(sWh + ks * 2 * LBO_I, LBO_I, 128, 0);
-                        tc::mma_bf16(tm + kColState, tc::sdesc(sBl + ks * 2048, kPanel, 1024, 2), dWh, idS,
-                                     ks > 0 ? 1u : acc0);
-                        tc::mma_bf16(tm + kColState, dBh, dWh, idS, 1);
-                        tc::mma_bf16(tm + kColState, dBh, tc::sdesc(sWl + ks * 2 * LBO_I, LBO_I, 128, 0), idS, 1);
+                    if (leader) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            if (ks < ksteps) {
+                                tc::mma_bf16(tm + kColState, dBlm + koff_m(ks), dWh + koff_i(ks), idS,
+                                             ks > 0 ? 1u : acc0);
+                                tc::mma_bf16(tm + kColState, dBhm + koff_m(ks), dWh + koff_i(ks), idS, 1);
+                                tc::mma_bf16(tm + kColState, dBhm + koff_m(ks), dWl + koff_i(ks), idS, 1);
+                            }
+                        }
                     }
+                    __syncwarp();
                 }
                 // the staged rows are consumed: stage the next chunk's (needed only
                 // at the next chunk's conv, so after this chunk's MMAs are queued)
-                if (has_next && ok1) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, c0 + Q);
+                if (has_next && ok1 && leader) stage_raw_x<TA, P>(&tmx, sRaw, bar_x, b, h, c0 + Q);
+                __syncwarp();
                 if (wait_ok(bar_op2, par, ERR_MBAR_TIMEOUT_MMA)) {
                     tc::tc_fence_after();
                     // phase 2: Y_diag += M x~ (onto D x~, M from TMEM)
-                    for (int ks = 0; ks < ksteps; ++ks)
-                        tc::mma_bf16_tmem_a(tm + kColYd, tm + kColG + (ks >> 2) * 64 + (ks & 3) * 8,
-                                            tc::sdesc(sX + ks * 2 * LBO_I, LBO_I, 128, 0), idY, 1);
-                    tc::mma_commit(bar_y);
+                    if (leader) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            if (ks < ksteps)
+                                tc::mma_bf16_tmem_a(tm + kColYd, tm + kColG + Parts::m_col(ks), dX + koff_i(ks), idY,
+                                                    1);
+                        tc::mma_commit(bar_y);
+                    }
+                    __syncwarp();
                 }
                 // every operand tile of this chunk is consumed: fetch the next chunk's
                 if (wait_ok(bar_y, par, ERR_MBAR_TIMEOUT_MMA) && has_next) {
-                    const uint8_t* nsrc = tiles_of(c + 1);
-                    tc::mbar_arrive_expect_tx(bar_a, 2 * kTileBytes);
-                    tc::bulk_g2s(sm + L::kBh, nsrc, kTileBytes, bar_a);
-                    tc::bulk_g2s(sm + L::kC, nsrc + 2 * kTileBytes, kTileBytes, bar_a);
-                    tc::mbar_arrive_expect_tx(bar_b, kTileBytes);
-                    tc::bulk_g2s(sm + L::kBl, nsrc + kTileBytes, kTileBytes, bar_b);
+                    if (leader) {
+                        const uint8_t* nsrc = tiles_of(c + 1);
+                        tc::mbar_arrive_expect_tx(bar_a, 2 * kTileBytes);
+                        tc::bulk_g2s(sm + L::kBh, nsrc, kTileBytes, bar_a);
+                        tc::bulk_g2s(sm + L::kC, nsrc + 2 * kTileBytes, kTileBytes, bar_a);
+                        tc::mbar_arrive_expect_tx(bar_b, kTileBytes);
+                        tc::bulk_g2s(sm + L::kBl, nsrc + kTileBytes, kTileBytes, bar_b);
+                    }
+                    __syncwarp();
                 }
             }
-            if (*sFlag) {
+            if (*sFlag && leader) {
                 // A wait gave up. Before the CTA frees TMEM and exits: every MMA
-                // this thread issued must be done (the commit arrives on bar_end
+                // this lane issued must be done (the commit arrives on bar_end
                 // once all of them have completed; some, such as Y_off and the
                 // state terms, are covered by no other commit), and the copies
                 // still in flight must land. Every wait here is bounded.
@@ -516,15 +658,17 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         if (state_in_tmem) {
             const int n = row;
 #pragma unroll
-            for (int q8 = 0; q8 < NQ; ++q8) {
-                const int p0 = half * PH + q8 * 8;
-                float v[8];
+            for (int k = 0; k < NU; ++k) {
+                if (k < nu) {
+                    const int p0 = (u0 + k) * 8;
+                    float v[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    v[q] = (a.init_ssm && n < s.N)
-                               ? __ldg(a.init_ssm + (((size_t)b * s.H + h) * P + p0 + q) * s.N + n)
-                               : 0.f;
-                tc::tmem_st8(tm + lane_base + kColState + p0, v);
+                    for (int q = 0; q < 8; ++q)
+                        v[q] = (a.init_ssm && n < s.N)
+                                   ? __ldg(a.init_ssm + (((size_t)b * s.H + h) * P + p0 + q) * s.N + n)
+                                   : 0.f;
+                    tc::tmem_st8(tm + lane_base + kColState + p0, v);
+                }
             }
             tc::tmem_wait_st();
         }
@@ -533,11 +677,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         // a chunk of Lx rows, and the column factor of the decay mask,
         // Eb_j = exp(S_j1 - S_j) dt_j with j1 = j | 7 the last column of j's
         // 8-column block (0 past the chunk end, where dt_j = 0), all into shared
-        // memory. S does not increase, so Eb_j <= dt_j. Every compute thread
-        // must call it (it holds barriers).
+        // memory by the dt part. S does not increase, so Eb_j <= dt_j. Every
+        // compute thread must call it (it holds barriers).
         auto dt_phase = [&](int Lx, float raw) {
             float v = 0.f, dt = 0.f;
-            if (half == 0) {
+            if (dt_part) {
                 dt = row < Lx ? softplus_f32(raw + dtb) : 0.f;
                 v = dt * A;
 #pragma unroll
@@ -545,18 +689,19 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
                     const float o = __shfl_up_sync(0xffffffffu, v, off);
                     if (lane >= off) v += o;
                 }
-                if (lane == 31) sWsum[warp] = v;
+                if (lane == 31) sWsum[quarter] = v;
             }
             compute_sync();
-            if (half == 0) {
+            if (dt_part) {
                 float add = 0.f;
-                for (int w = 0; w < (row >> 5); ++w) add += sWsum[w];
+                for (int w = 0; w < quarter; ++w) add += sWsum[w];
                 const float S = v + add;
+                const float S1 = __shfl_sync(0xffffffffu, S, lane | 7);  // same warp: 8 | 32
                 sS[row] = S;
                 sDt[row] = dt;
+                sEb[row] = ex2_approx((S1 - S) * kLog2e) * dt;
             }
             compute_sync();
-            if (half == 0) sEb[row] = ex2_approx((sS[row | 7] - sS[row]) * kLog2e) * sDt[row];
         };
 
         // y = (D x~ + M x~) + exp(S_i) Y_off for the chunk whose results sit in TMEM.
@@ -565,28 +710,28 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         auto y_epilogue = [&](int c0y, int Ly, float eSy, uint32_t colYo) {
             const bool live = row < Ly;
             const size_t ybase = (((size_t)b * T + c0y + row) * s.H + h) * P;
-            float yd[NQ][8], yo[NQ][8];
 #pragma unroll
-            for (int q8 = 0; q8 < NQ; ++q8) {
-                tc::tmem_ld8(tm + lane_base + kColYd + half * PH + q8 * 8, yd[q8]);
-                tc::tmem_ld8(tm + lane_base + colYo + half * PH + q8 * 8, yo[q8]);
-            }
-            tc::tmem_wait_ld();
+            for (int k = 0; k < NU; ++k) {
+                if (k < nu) {
+                    const int p0 = (u0 + k) * 8;
+                    float yd[8], yo[8];
+                    tc::tmem_ld8(tm + lane_base + kColYd + p0, yd);
+                    tc::tmem_ld8(tm + lane_base + colYo + p0, yo);
+                    tc::tmem_wait_ld();
+                    float2 out[4];
 #pragma unroll
-            for (int q8 = 0; q8 < NQ; ++q8) {
-                const int p0 = half * PH + q8 * 8;
-                float out[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) out[q] = fmaf(eSy, yo[q8][q], yd[q8][q]);
-                if (live) {
-                    if constexpr (sizeof(TA) == 2) {
-                        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.y) + ybase + p0) =
-                            make_uint4(pack2(out[0], out[1]), pack2(out[2], out[3]), pack2(out[4], out[5]),
-                                       pack2(out[6], out[7]));
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + ybase + p0);
-                        dst[0] = make_float4(out[0], out[1], out[2], out[3]);
-                        dst[1] = make_float4(out[4], out[5], out[6], out[7]);
+                    for (int m = 0; m < 4; ++m)
+                        out[m] = f2_fma(f2_splat(eSy), make_float2(yo[2 * m], yo[2 * m + 1]),
+                                        make_float2(yd[2 * m], yd[2 * m + 1]));
+                    if (live) {
+                        if constexpr (sizeof(TA) == 2) {
+                            *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.y) + ybase + p0) =
+                                make_uint4(pack2(out[0]), pack2(out[1]), pack2(out[2]), pack2(out[3]));
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + ybase + p0);
+                            dst[0] = make_float4(out[0].x, out[0].y, out[1].x, out[1].y);
+                            dst[1] = make_float4(out[2].x, out[2].y, out[3].x, out[3].y);
+                        }
                     }
                 }
             }
@@ -595,7 +740,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
         if (nchb > 0) {
             dt_phase(min(Q, Tb), raw_to_f32<TA>(dt_raw_bits));
             dt_raw_bits = 0;
-            if (half == 0 && nchb > 1 && row < min(Q, Tb - Q))
+            if (dt_part && nchb > 1 && row < min(Q, Tb - Q))
                 dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + Q + row) * a.fdt + h);
         }
 
@@ -619,31 +764,37 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             //    overwrites the accumulator.
             const float Slast = sS[Lc - 1];
             {
-                const float decay = __expf(Slast);
+                const float2 decay = f2_splat(__expf(Slast));
                 const int n = row;
                 const bool in_tmem = c > 0 || state_in_tmem;
-                float v[NQ][8];
+                float v[NU][8];
                 if (in_tmem) {
 #pragma unroll
-                    for (int q8 = 0; q8 < NQ; ++q8)
-                        tc::tmem_ld8(tm + lane_base + kColState + half * PH + q8 * 8, v[q8]);
+                    for (int k = 0; k < NU; ++k)
+                        if (k < nu) tc::tmem_ld8(tm + lane_base + kColState + (u0 + k) * 8, v[k]);
                     tc::tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int q8 = 0; q8 < NQ; ++q8)
+                    for (int k = 0; k < NU; ++k)
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) v[q8][q] = 0.f;
+                        for (int q = 0; q < 8; ++q) v[k][q] = 0.f;
                 }
 #pragma unroll
-                for (int q8 = 0; q8 < NQ; ++q8) {
-                    const int p0 = half * PH + q8 * 8;
-                    *reinterpret_cast<uint4*>(sm + L::kH + tc::mn_inter_off(p0, n, P)) =
-                        make_uint4(pack2(v[q8][0], v[q8][1]), pack2(v[q8][2], v[q8][3]), pack2(v[q8][4], v[q8][5]),
-                                   pack2(v[q8][6], v[q8][7]));
-                    if (in_tmem) {
+                for (int k = 0; k < NU; ++k) {
+                    if (k < nu) {
+                        const int p0 = (u0 + k) * 8;
+                        *reinterpret_cast<uint4*>(sm + L::kH + tc::mn_inter_off(p0, n, P)) =
+                            make_uint4(pack2(v[k][0], v[k][1]), pack2(v[k][2], v[k][3]), pack2(v[k][4], v[k][5]),
+                                       pack2(v[k][6], v[k][7]));
+                        if (in_tmem) {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) v[q8][q] *= decay;
-                        tc::tmem_st8(tm + lane_base + kColState + p0, v[q8]);
+                            for (int m = 0; m < 4; ++m) {
+                                const float2 sc = f2_mul(make_float2(v[k][2 * m], v[k][2 * m + 1]), decay);
+                                v[k][2 * m] = sc.x;
+                                v[k][2 * m + 1] = sc.y;
+                            }
+                            tc::tmem_st8(tm + lane_base + kColState + p0, v[k]);
+                        }
                     }
                 }
                 if (in_tmem) tc::tmem_wait_st();
@@ -655,7 +806,6 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
 
             // 2a. this chunk's staged x rows
             wait_ok(bar_x, par, ERR_MBAR_TIMEOUT_LOAD);
-            compute_sync();
             if (c == 0 && a.init_conv) {
                 // frames -3..-1 (zero-filled by the copy) come from the initial conv tail
                 constexpr int V = L::kRowData / 16;
@@ -671,47 +821,50 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             const float Si = sS[row];
             const float wi = row < Lc ? __expf(Slast - Si) * sDt[row] : 0.f;
 
-            // 2. conv + SiLU of this head's x channels for row i (staged rows i..i+3)
-            float xf[PH];
+            // 2. conv + SiLU of this part's x channels for row i (staged rows
+            //    i..i+3), on channel pairs
+            float2 xf[NU][4];
 #pragma unroll
-            for (int q8 = 0; q8 < NQ; ++q8) {
-                const int p0 = half * PH + q8 * 8;
-                float o[8];
-                if (row < Lc) {
-                    Act8<TA> v[4];
+            for (int k = 0; k < NU; ++k) {
+                if (k < nu) {
+                    const int p0 = (u0 + k) * 8;
+                    float2 o[4];
+                    if (row < Lc) {
+                        const float4 b0 = *reinterpret_cast<const float4*>(sCb + p0);
+                        const float4 b1 = *reinterpret_cast<const float4*>(sCb + p0 + 4);
+                        float2 acc[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                                         make_float2(b1.z, b1.w)};
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) v[k].load_rw(sRaw + (size_t)(row + k) * L::kRowBytes, p0);
-                    const float4 b0 = reinterpret_cast<const float4*>(sCb + p0)[0];
-                    const float4 b1 = reinterpret_cast<const float4*>(sCb + p0)[1];
+                        for (int tap = 0; tap < 4; ++tap) {
+                            float2 xv[4];
+                            load8_pairs<TA>(sRaw + (size_t)(row + tap) * L::kRowBytes + p0 * sizeof(TA), xv);
+                            const float4 w0 = *reinterpret_cast<const float4*>(sCw + tap * P + p0);
+                            const float4 w1 = *reinterpret_cast<const float4*>(sCw + tap * P + p0 + 4);
+                            acc[0] = f2_fma(make_float2(w0.x, w0.y), xv[0], acc[0]);
+                            acc[1] = f2_fma(make_float2(w0.z, w0.w), xv[1], acc[1]);
+                            acc[2] = f2_fma(make_float2(w1.x, w1.y), xv[2], acc[2]);
+                            acc[3] = f2_fma(make_float2(w1.z, w1.w), xv[3], acc[3]);
+                        }
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float4 w = reinterpret_cast<const float4*>(sCw)[p0 + j];
-                        float acc = j < 4 ? (&b0.x)[j] : (&b1.x)[j - 4];
-                        acc = fmaf(w.x, v[0].get(j), acc);
-                        acc = fmaf(w.y, v[1].get(j), acc);
-                        acc = fmaf(w.z, v[2].get(j), acc);
-                        acc = fmaf(w.w, v[3].get(j), acc);
-                        o[j] = silu_fast(acc);
+                        for (int m = 0; m < 4; ++m) o[m] = silu2(acc[m]);
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) o[m] = make_float2(0.f, 0.f);
                     }
-                } else {
+                    uint32_t xh[4], wh[4], wl[4];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) o[j] = 0.f;
+                    for (int m = 0; m < 4; ++m) {
+                        xf[k][m] = o[m];
+                        xh[m] = pack2(o[m]);
+                        const float2 w = f2_mul(o[m], f2_splat(wi));
+                        wh[m] = pack2(w);
+                        wl[m] = pack2(f2_sub(w, bf2_to_f2(wh[m])));
+                    }
+                    const uint32_t off = tc::mn_inter_off(p0, row, P);
+                    *reinterpret_cast<uint4*>(sm + L::kX + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+                    *reinterpret_cast<uint4*>(sm + L::kWh + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                    *reinterpret_cast<uint4*>(sm + L::kWl + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                 }
-                uint32_t xh[4], wh[4], wl[4];
-#pragma unroll
-                for (int j = 0; j < 8; j += 2) {
-                    xf[q8 * 8 + j] = o[j];
-                    xf[q8 * 8 + j + 1] = o[j + 1];
-                    xh[j / 2] = pack2(o[j], o[j + 1]);
-                    const float w0 = wi * o[j], w1 = wi * o[j + 1];
-                    const uint32_t hw = pack2(w0, w1);
-                    wh[j / 2] = hw;
-                    wl[j / 2] = pack2(w0 - __uint_as_float(hw << 16), w1 - __uint_as_float(hw & 0xFFFF0000u));
-                }
-                const uint32_t off = tc::mn_inter_off(p0, row, P);
-                *reinterpret_cast<uint4*>(sm + L::kX + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
-                *reinterpret_cast<uint4*>(sm + L::kWh + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-                *reinterpret_cast<uint4*>(sm + L::kWl + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
             }
 
             // hand the phase-1 operands (x~ and w o x~ tiles) to the control warp
@@ -719,73 +872,84 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             tc::tc_fence_before();
             tc::mbar_arrive(bar_op1);
 
-            // 4. meanwhile: the previous chunk's y (this chunk's MMAs so far write
+            // 3. meanwhile: the previous chunk's y (this chunk's MMAs so far write
             //    G, the state and the other Y_off buffer), then this chunk's D x~
             //    preloaded into the Y_diag accumulator that phase 2 adds M x~ onto
             if (c > 0) y_epilogue(c0_prev, L_prev, eS_prev, par ? kColYo0 : kColYo1);
-            {
-                float dx[8];
 #pragma unroll
-                for (int q8 = 0; q8 < NQ; ++q8) {
+            for (int k = 0; k < NU; ++k) {
+                if (k < nu) {
+                    float dx[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) dx[q] = Dh * xf[q8 * 8 + q];
-                    tc::tmem_st8(tm + lane_base + kColYd + half * PH + q8 * 8, dx);
+                    for (int m = 0; m < 4; ++m) {
+                        const float2 d = f2_mul(xf[k][m], f2_splat(Dh));
+                        dx[2 * m] = d.x;
+                        dx[2 * m + 1] = d.y;
+                    }
+                    tc::tmem_st8(tm + lane_base + kColYd + (u0 + k) * 8, dx);
                 }
-                tc::tmem_wait_st();
             }
-            wait_ok(bar_g, par, ERR_MBAR_TIMEOUT_MMA);
-            tc::tc_fence_after();
+            tc::tmem_wait_st();
 
-            // 5. M = G o exp(S_i - S_j) dt_j (j <= i) -> bf16 into TMEM, the A
-            //    operand of Y_diag (the state MMAs run meanwhile).
+            // 4. M = G o exp(S_i - S_j) dt_j (j <= i) -> bf16 into TMEM, the A
+            //    operand of Y_diag (the state MMAs run meanwhile), by the parts
+            //    that own mask columns, 16 columns j (one K-step) at a time. Each
+            //    K-step is, for the whole warp (rows 32 quarter .. +31), either
+            //    left of every row's diagonal block, holding some row's
+            //    diagonal block, or right of every row's diagonal (zero).
             //    An 8-column block [j0, j1] wholly left of row i factors as
-            //    exp(S_i - S_j1) * Eb_j, both factors <= 1 (S does not increase);
-            //    the block holding the diagonal takes one exponential per entry.
-            {
+            //    exp(S_i - S_j1) * Eb_j, both factors <= 1 (S does not
+            //    increase); the block holding the diagonal takes one exponential
+            //    per entry.
+            const int nks = Parts::mask_steps(part);
+            if (nks > 0) {
+                wait_ok(bar_g, par, ERR_MBAR_TIMEOUT_MMA);
+                tc::tc_fence_after();
+                const int fks = Parts::first_mask_step(part);
                 const int i = row;
                 const bool live = i < Lc;
-                const int jd = i & ~7;                 // this row's diagonal block
-                const bool dg_here = (jd >> 6) == half;  // uniform across the warp
-                float dg[8];
+                const int jd = i & ~7;  // this row's diagonal block
 #pragma unroll
-                for (int e = 0; e < 8; ++e) dg[e] = 0.f;
-                if (dg_here && live) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        if (jd + e <= i) dg[e] = ex2_approx((Si - sS[jd + e]) * kLog2e) * sDt[jd + e];
-                }
-                float gv[4][16];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) tc::tmem_ld16(tm + lane_base + kColG + half * 64 + q * 16, gv[q]);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int j0 = half * 64 + q * 16;
-                    uint32_t pk[8];
-#pragma unroll
-                    for (int e8 = 0; e8 < 16; e8 += 8) {
-                        const int jb = j0 + e8;
-                        // row factor of a block left of the diagonal (0 for dead rows)
-                        const float ea = (live && jb < jd) ? ex2_approx((Si - sS[jb + 7]) * kLog2e) : 0.f;
-                        const float4 c0 = *reinterpret_cast<const float4*>(sEb + jb);
-                        const float4 c1 = *reinterpret_cast<const float4*>(sEb + jb + 4);
-                        float m[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float eb = e < 4 ? (&c0.x)[e] : (&c1.x)[e - 4];
-                            m[e] = gv[q][e8 + e] * (jb == jd ? dg[e] : eb * ea);
-                        }
-                        pk[e8 / 2 + 0] = pack2(m[0], m[1]);
-                        pk[e8 / 2 + 1] = pack2(m[2], m[3]);
-                        pk[e8 / 2 + 2] = pack2(m[4], m[5]);
-                        pk[e8 / 2 + 3] = pack2(m[6], m[7]);
-                    }
-                    // columns j0 .. j0+15 of row i: 8 TMEM columns over G columns
-                    // this thread has read (all of them are in gv)
+                for (int q = 0; q < NK; ++q) {
+                    const int j0 = 16 * (fks + q);
                     float mv[8];
+                    if (j0 >= 32 * quarter + 32) {
+                        // right of every row's diagonal: zero
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) mv[e] = __uint_as_float(pk[e]);
-                    tc::tmem_st8(tm + lane_base + kColG + half * 64 + q * 8, mv);
+                        for (int e = 0; e < 8; ++e) mv[e] = 0.f;
+                    } else {
+                        float gv[16];
+                        tc::tmem_ld16(tm + lane_base + kColG + j0, gv);
+                        const bool left = j0 + 16 <= 32 * quarter;  // uniform across the warp
+                        // this row's diagonal block, when it lies in this K-step
+                        float dg[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) dg[e] = 0.f;
+                        if (!left && live && jd >= j0 && jd < j0 + 16) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                if (jd + e <= i) dg[e] = ex2_approx((Si - sS[jd + e]) * kLog2e) * sDt[jd + e];
+                        }
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int e8 = 0; e8 < 16; e8 += 8) {
+                            const int jb = j0 + e8;
+                            // row factor of a block left of the diagonal (0 for dead rows)
+                            const float ea = (live && jb < jd) ? ex2_approx((Si - sS[jb + 7]) * kLog2e) : 0.f;
+                            const float4 c0v = *reinterpret_cast<const float4*>(sEb + jb);
+                            const float4 c1v = *reinterpret_cast<const float4*>(sEb + jb + 4);
+                            float2 f[4] = {make_float2(c0v.x, c0v.y), make_float2(c0v.z, c0v.w),
+                                           make_float2(c1v.x, c1v.y), make_float2(c1v.z, c1v.w)};
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                f[m] = f2_mul(f[m], f2_splat(ea));
+                                if (!left && jb == jd) f[m] = make_float2(dg[2 * m], dg[2 * m + 1]);
+                                const float2 mm = f2_mul(make_float2(gv[e8 + 2 * m], gv[e8 + 2 * m + 1]), f[m]);
+                                mv[e8 / 2 + m] = __uint_as_float(pack2(mm));
+                            }
+                        }
+                    }
+                    tc::tmem_st8(tm + lane_base + kColG + Parts::m_col(fks + q), mv);
                 }
                 tc::tmem_wait_st();
             }
@@ -793,12 +957,13 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
             tc::tc_fence_before();
             tc::mbar_arrive(bar_op2);
 
-            // 6. meanwhile: the next chunk's dt phase (the mask above was the last
-            //    reader of this chunk's S, dt and Eb; S_i is kept in a register)
+            // 5. meanwhile: the next chunk's dt phase (its first barrier orders this
+            //    chunk's reads of S, dt and Eb before its writes; S_i is kept in a
+            //    register)
             if (has_next) {
                 dt_phase(Ln, raw_to_f32<TA>(dt_raw_bits));
                 dt_raw_bits = 0;
-                if (half == 0 && row < Lnn)
+                if (dt_part && row < Lnn)
                     dt_raw_bits = load_raw_pinned<TA>(a.dt_raw, ((size_t)b * T + c0 + 2 * Q + row) * a.fdt + h);
             }
             wait_ok(bar_y, par, ERR_MBAR_TIMEOUT_MMA);
@@ -820,16 +985,19 @@ __global__ void __launch_bounds__(kSsdThreads, 1) scan_ssd_kernel(ScanArgs a, in
     // final state: TMEM [n][p] -> final_ssm [b,h,p,n]
     if (ok && compute) {
         const int n = row;
-        float v[NQ][8];
 #pragma unroll
-        for (int q8 = 0; q8 < NQ; ++q8) tc::tmem_ld8(tm + lane_base + kColState + half * PH + q8 * 8, v[q8]);
-        tc::tmem_wait_ld();
-        if (n < s.N) {
+        for (int k = 0; k < NU; ++k) {
+            if (k < nu) {
+                const int p0 = (u0 + k) * 8;
+                float v[8];
+                tc::tmem_ld8(tm + lane_base + kColState + p0, v);
+                tc::tmem_wait_ld();
+                if (n < s.N) {
 #pragma unroll
-            for (int q8 = 0; q8 < NQ; ++q8)
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    a.final_ssm[(((size_t)b * s.H + h) * P + half * PH + q8 * 8 + q) * s.N + n] = v[q8][q];
+                    for (int q = 0; q < 8; ++q)
+                        a.final_ssm[(((size_t)b * s.H + h) * P + p0 + q) * s.N + n] = v[q];
+                }
+            }
         }
     }
     tc::tc_fence_before();

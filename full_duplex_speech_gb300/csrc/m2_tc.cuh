@@ -61,6 +61,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     return true;
 }
 
+// True in exactly one lane of the (converged) calling warp.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ------------------------------------------------------------- bulk copies
 // 1-D bulk copy global -> shared (the TMA engine), completion counted on `bar`
 // in bytes. dst, src 16-byte aligned; bytes a multiple of 16.
