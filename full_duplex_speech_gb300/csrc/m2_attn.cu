@@ -14,19 +14,26 @@
 // kv head in bf16 against 4R flops per byte.
 //
 // Two kernels, both launched with programmatic dependent launch:
-//  1. attn_split_kernel: one CTA per (chunk of up to 128 positions, kv head,
-//     session; shorter chunks where there would be too few CTAs to fill the
-//     GPU). Two bulk copies (the TMA engine) bring the chunk's cached keys
-//     and values into shared memory: each is one contiguous run of rows. The
-//     chunk holding position len[s] takes the new key and value from the
-//     inputs instead, and writes them into the cache there (no other CTA
-//     reads that slot). Then scores (8 lanes per position, 16 dims a lane, the
-//     R heads' dot products reduced over the 8 lanes, q held in fp32
-//     registers), the chunk's softmax statistics in the log2 domain (m = max,
-//     l = sum of 2^(a - m)) and acc = sum_t 2^(a_t - m) v_t (16 threads per
-//     value row, 8 dims each, all R heads at once), written as the chunk's
-//     partial result.
-//  2. attn_combine_kernel: per (kv head, session), merges the chunks:
+//  1. a split kernel that computes partial results over runs of positions:
+//     - bf16 caches: attn_walk_kernel, on the tensor cores. One CTA per
+//       (walker, kv head, session): a walker takes a run of 64-position
+//       chunks, brought into shared memory by 2-D TMA copies through a
+//       3-stage ring; its four warps keep their own online softmax over 16
+//       positions of every chunk, with the scores (query heads x positions)
+//       and the weighted values (query heads x dims) as mma.sync products.
+//     - fp32 caches: attn_split_kernel, on the CUDA cores. One CTA per (chunk
+//       of up to 64 positions, kv head, session; shorter chunks where there
+//       would be too few CTAs to fill the GPU). Two bulk copies (the TMA
+//       engine) bring the chunk's cached keys and values into shared memory;
+//       then scores (8 lanes per position, 16 dims a lane, the R heads' dot
+//       products reduced over the 8 lanes, q held in fp32 registers), the
+//       chunk's softmax statistics in the log2 domain (m = max, l = sum of
+//       2^(a - m)) and acc = sum_t 2^(a_t - m) v_t (16 threads per value row,
+//       8 dims each, all R heads at once), written as the chunk's partial result.
+//     The run holding position len[s] takes the new key and value from the
+//     inputs instead of the cache, and writes them into the cache there (no
+//     other CTA reads that slot).
+//  2. attn_combine_kernel: per (kv head, session), merges the partial results:
 //     M = max_i m_i, out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.
 #include "m2_common.cuh"
 #include "m2_launch.h"
@@ -65,7 +72,16 @@ __host__ __device__ inline int attn_chunks(int Tmax, int tc) { return (Tmax + tc
 // grid would have fewer than two CTAs per SM of the 152-SM GB300, so that a
 // short cache of few sessions still spreads over the GPU. A function of the
 // sizes alone: the workspace query needs no device.
+int attn_walk_chunks(int S, int Hkv, int Tmax);
+
+// bf16 caches go to the tensor-core walkers, whose 2-D copies address the
+// caches' rows (S x Hkv x Tmax of them) with 32-bit coordinates.
+bool attn_use_walk(int S, int Hkv, int Tmax, bool bf16) {
+    return bf16 && (long long)S * Hkv * Tmax < (1LL << 31) - 64;
+}
+
 int attn_chunk_len(int S, int Hkv, int Tmax, bool bf16) {
+    if (attn_use_walk(S, Hkv, Tmax, bf16)) return attn_walk_chunks(S, Hkv, Tmax) * 64;  // a walker's run of 64-position chunks
     int tc = bf16 ? AttnTile<bf16_t>::kTc : AttnTile<float>::kTc;
     while (tc > 32 && (long)S * Hkv * attn_chunks(Tmax, tc) < 2 * 152) tc /= 2;
     return tc;
@@ -392,6 +408,289 @@ __global__ void __launch_bounds__(kAttnMaxR * 64) attn_combine_kernel(AttnArgs a
     }
 }
 
+// ---------------------------------------------------------------------------
+// bf16 caches: the split kernel on the tensor cores. A CTA ("walker") takes a
+// run of consecutive 64-position chunks of one (session, kv head); a 3-stage
+// ring of 2-D TMA copies (128-byte swizzle) keeps the next chunks' keys and
+// values in flight while it computes. Each of its four warps takes 16
+// positions of every chunk and keeps its own online softmax, so the warps
+// meet only at the chunk boundary where a stage is refilled:
+//     scores  S (16 x 16) = Q (16 query rows, R real) . K^T      mma m16n8k16
+//     P = 2^(S log2e scale - m), m the running max, l += sum P
+//     acc (16 x 128) += P . V      (P as bf16 hi + lo: two MMAs)
+// The scores' accumulator fragments are the P operand's fragments as they
+// stand (row = query head, column = position). The four warps' (m, l, acc)
+// are merged at the end into the walker's partial result, which the combine
+// kernel merges with the other walkers' as it does the chunks'.
+constexpr int kWalkTc = 64;                        // positions per chunk
+constexpr int kWalkStages = 3;
+constexpr int kWalkThreads = 128;
+constexpr uint32_t kWalkBox = kWalkTc * 128;        // one box: 64 rows x 64 dims of bf16 (8 KiB)
+constexpr uint32_t kWalkStage = 4 * kWalkBox;       // K (2 boxes) + V (2 boxes)
+constexpr uint32_t kWalkBar = kWalkStages * kWalkStage;
+constexpr uint32_t kWalkSmem = kWalkBar + 64 + 1024;  // + barriers, + slack to align to 1024
+
+// Byte offset of (row r, dim d) in a stage's K or V tile: two 64-dim boxes,
+// 128-byte rows, the 16-byte pieces of a row XOR-ed with r % 8.
+__device__ __forceinline__ uint32_t walk_off(int r, int d) {
+    return (uint32_t)(d >> 6) * kWalkBox + (uint32_t)r * 128u + ((((uint32_t)(d & 63) >> 3) ^ (uint32_t)(r & 7)) << 4) +
+           ((uint32_t)(d & 7) << 1);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+// d += A B, m16n8k16, bf16 in, fp32 accumulate; A's rows 8..15 are zero here
+__device__ __forceinline__ void mma_rows8(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__global__ void __launch_bounds__(kWalkThreads, 2) attn_walk_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmk,
+                                                                    const __grid_constant__ CUtensorMap tmv, int cpw) {
+    extern __shared__ uint8_t walk_smem_raw[];
+    uint8_t* sm = walk_smem_raw + ((1024u - (tc::smem_u32(walk_smem_raw) & 1023u)) & 1023u);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kWalkBar);  // one per stage: its copies landed
+    const int wk = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, t = lane & 3;  // fragment row (query head) and lane in its quad
+    const int R = a.Hq / a.Hkv;
+    constexpr int RB = kAttnD * 2;  // bytes of one cached row
+
+    pdl_wait();  // the inputs and the caches may come from the previous kernel
+    pdl_trigger();
+    const int len = a.lens[s] + a.len_add;
+    if (len < 0 || len >= a.Tmax) return;  // refused; the combine kernel reports it
+    const int nch = len / kWalkTc + 1;     // chunks holding positions 0 .. len
+    const int cb = wk * cpw, ce = min(cb + cpw, nch);
+    if (cb >= ce) return;                  // past this session's positions
+    const int row0 = (s * a.Hkv + g) * a.Tmax;  // tensor row of position 0
+
+    auto issue = [&](int c) {  // one thread: chunk c's keys and values into its stage
+        const int st = (c - cb) % kWalkStages;
+        uint8_t* dst = sm + st * kWalkStage;
+        tc::mbar_arrive_expect_tx(bar + st, kWalkStage);
+        const int y = row0 + c * kWalkTc;
+        tc::tma_load_2d(dst, &tmk, 0, y, bar + st);
+        tc::tma_load_2d(dst + kWalkBox, &tmk, 64, y, bar + st);
+        tc::tma_load_2d(dst + 2 * kWalkBox, &tmv, 0, y, bar + st);
+        tc::tma_load_2d(dst + 3 * kWalkBox, &tmv, 64, y, bar + st);
+    };
+    if (tid == 0) {
+        for (int i = 0; i < kWalkStages; ++i) tc::mbar_init(bar + i, 1);
+        tc::fence_mbar_init();
+        for (int c = cb; c < min(ce, cb + kWalkStages); ++c) issue(c);
+    }
+    // the query rows as the A operand (row = query head gq of this kv head;
+    // rows past R, and rows 8..15, zero): per 16-dim K-step two bf16 pairs
+    uint32_t qa[8][2];
+    {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(a.q) +
+                                                                 (size_t)s * a.q_ss + (size_t)(g * R + min(gq, R - 1)) * kAttnD);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            qa[kk][0] = gq < R ? __ldg(qrow + 8 * kk + t) : 0u;
+            qa[kk][1] = gq < R ? __ldg(qrow + 8 * kk + 4 + t) : 0u;
+        }
+    }
+    const float sl2 = a.scale * kLog2e;
+    float m = -1e30f, l = 0.f;  // running max (finite: a fully masked row stays harmless) and sum
+    float acc[16][4];
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[dt][e] = 0.f;
+    __syncthreads();  // the barriers are initialised
+
+    bool ok = true;
+    for (int c = cb; c < ce; ++c) {
+        const int st = (c - cb) % kWalkStages;
+        const uint32_t phase = ((c - cb) / kWalkStages) & 1;
+        uint8_t* sK = sm + st * kWalkStage;
+        uint8_t* sV = sK + 2 * kWalkBox;
+        if (!tc::mbar_wait(bar + st, phase)) {
+            atomicOr(a.err, ERR_MBAR_TIMEOUT_LOAD);
+            ok = false;
+        }
+        if (c == nch - 1) {
+            // the chunk holding position len: the new key and value go into
+            // their rows here and into the caches; the value rows past len
+            // (whatever the cache holds there) become zeros
+            const int pl = len - c * kWalkTc;
+            if (tid < 32) {
+                const int which = tid >> 4, piece = tid & 15;
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(which ? a.v_new : a.k_new) +
+                                     ((size_t)s * a.kv_ss + (size_t)g * kAttnD) * 2 + piece * 16;
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+                *reinterpret_cast<uint4*>((which ? sV : sK) + walk_off(pl, piece * 8)) = v;
+                uint8_t* dst = reinterpret_cast<uint8_t*>(which ? a.v_cache : a.k_cache) + ((size_t)row0 + len) * RB +
+                               piece * 16;
+                *reinterpret_cast<uint4*>(dst) = v;
+            }
+            for (int e = tid; e < (kWalkTc - 1 - pl) * 16; e += kWalkThreads) {
+                const int r = pl + 1 + e / 16, piece = e % 16;
+                *reinterpret_cast<uint4*>(sV + walk_off(r, piece * 8)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncthreads();
+        }
+        const uint32_t kb = tc::smem_u32(sK), vb = tc::smem_u32(sV);
+        // scores of this warp's positions 16 warp .. +15 (two 8-position tiles)
+        float sc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+            const int r = 16 * warp + 8 * nt + (lane & 7);
+#pragma unroll
+            for (int kk2 = 0; kk2 < 4; ++kk2) {
+                uint32_t b[4];
+                ldsm_x4(kb + walk_off(r, 32 * kk2 + 8 * (lane >> 3)), b);
+                mma_rows8(sc[nt], qa[2 * kk2][0], qa[2 * kk2][1], b[0], b[1]);
+                mma_rows8(sc[nt], qa[2 * kk2 + 1][0], qa[2 * kk2 + 1][1], b[2], b[3]);
+            }
+        }
+        // online softmax of row gq over these 16 positions (-inf past len)
+        float sv[2][2], mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int pos = c * kWalkTc + 16 * warp + 8 * nt + 2 * t + e;
+                sv[nt][e] = (pos <= len && gq < R) ? sc[nt][e] * sl2 : -INFINITY;
+                mx = fmaxf(mx, sv[nt][e]);
+            }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m, mx);
+        const float corr = ex2_approx(m - mn);
+        m = mn;
+        float p[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) p[nt][e] = ex2_approx(sv[nt][e] - mn);  // 0 for -inf
+        l = fmaf(l, corr, (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]));
+#pragma unroll
+        for (int dt = 0; dt < 16; ++dt) {
+            acc[dt][0] *= corr;
+            acc[dt][1] *= corr;
+        }
+        // P as bf16 hi + lo (p = hi + lo to ~2^-16): row gq, positions 2t, 2t+1 and 8+2t, 8+2t+1
+        const uint32_t h0 = pack_bf16x2(p[0][0], p[0][1]), h1 = pack_bf16x2(p[1][0], p[1][1]);
+        const uint32_t l0 = pack_bf16x2(p[0][0] - __uint_as_float(h0 << 16), p[0][1] - __uint_as_float(h0 & 0xFFFF0000u));
+        const uint32_t l1 = pack_bf16x2(p[1][0] - __uint_as_float(h1 << 16), p[1][1] - __uint_as_float(h1 & 0xFFFF0000u));
+        // acc += P V: 16 tiles of 8 dims, two per transposed 4-matrix load
+        const int vr = 16 * warp + 8 * ((lane >> 3) & 1) + (lane & 7);
+#pragma unroll
+        for (int dt2 = 0; dt2 < 8; ++dt2) {
+            uint32_t b[4];
+            ldsm_x4_trans(vb + walk_off(vr, 16 * dt2 + 8 * (lane >> 4)), b);
+            mma_rows8(acc[2 * dt2], h0, h1, b[0], b[1]);
+            mma_rows8(acc[2 * dt2], l0, l1, b[0], b[1]);
+            mma_rows8(acc[2 * dt2 + 1], h0, h1, b[2], b[3]);
+            mma_rows8(acc[2 * dt2 + 1], l0, l1, b[2], b[3]);
+        }
+        __syncthreads();  // every warp is done with this stage
+        if (tid == 0 && ok && c + kWalkStages < ce) issue(c + kWalkStages);
+    }
+    if (!ok) {
+        // a copy did not land in time: let the copies still in flight land
+        // (bounded), leave no partial result (the combine kernel would read
+        // garbage: the error word is set)
+        if (tid == 0)
+            for (int i = 0; i < kWalkStages; ++i) tc::mbar_wait(bar + i, 0, 100000000ull), tc::mbar_wait(bar + i, 1, 100000000ull);
+        return;
+    }
+    // merge the four warps: the quad's sum of l, then (m, l, acc) through
+    // shared memory (over the stages, no longer read)
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    float* sml = reinterpret_cast<float*>(sm);                 // [4 warps][8 rows][2]
+    float* sacc = sml + 4 * 8 * 2;                             // [4 warps][8 rows][128]
+    if (t == 0) {
+        sml[(warp * 8 + gq) * 2] = m;
+        sml[(warp * 8 + gq) * 2 + 1] = l;
+    }
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt)
+        *reinterpret_cast<float2*>(sacc + (warp * 8 + gq) * kAttnD + 8 * dt + 2 * t) = make_float2(acc[dt][0], acc[dt][1]);
+    __syncthreads();
+    const size_t part = ((size_t)s * a.Hkv + g) * attn_chunks(a.Tmax, cpw * kWalkTc) + wk;
+    float* wacc = a.ws + part * R * kAttnD;
+    float* wml = a.ws + (size_t)a.S * a.Hkv * attn_chunks(a.Tmax, cpw * kWalkTc) * R * kAttnD + part * R * 2;
+    for (int r = 0; r < R; ++r) {
+        float M = -1e30f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, sml[(w * 8 + r) * 2]);
+        float o = 0.f, L = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float f = ex2_approx(sml[(w * 8 + r) * 2] - M);
+            o = fmaf(f, sacc[(w * 8 + r) * kAttnD + tid], o);
+            L = fmaf(f, sml[(w * 8 + r) * 2 + 1], L);
+        }
+        wacc[r * kAttnD + tid] = o;
+        if (tid == 0) *reinterpret_cast<float2*>(wml + 2 * r) = make_float2(M, L);
+    }
+}
+
+// Chunks per walker for bf16 caches: enough walkers that sessions x kv heads
+// x walkers fill two CTAs an SM of the 152-SM GB300 (a function of the sizes
+// alone, like the workspace query that depends on it).
+int attn_walk_chunks(int S, int Hkv, int Tmax) {
+    const long nchunks = (Tmax + kWalkTc - 1) / kWalkTc;
+    const long pairs = (long)S * Hkv;
+    const long walkers = pairs >= 2 * 152 ? 1 : (2 * 152 + pairs - 1) / pairs;
+    return (int)((nchunks + walkers - 1) / walkers);
+}
+
+cudaError_t make_cache_map(const void* cache, const AttnArgs& a, CUtensorMap* map) {
+    tc::EncodeTiledFn enc = tc::encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)kAttnD, (cuuint64_t)a.S * a.Hkv * a.Tmax};
+    const cuuint64_t strides[1] = {(cuuint64_t)kAttnD * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kWalkTc};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_walk(const AttnArgs& a, cudaStream_t st) {
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(attn_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWalkSmem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    CUtensorMap tmk, tmv;
+    e = make_cache_map(a.k_cache, a, &tmk);
+    if (e == cudaSuccess) e = make_cache_map(a.v_cache, a, &tmv);
+    if (e != cudaSuccess) return e;
+    const int cpw = a.tc / kWalkTc;
+    const int nwalk = attn_chunks(a.Tmax, a.tc);
+    return launch_pdl(attn_walk_kernel, dim3(nwalk, a.Hkv, a.S), dim3(kWalkThreads), kWalkSmem, st, a, tmk, tmv, cpw);
+}
+
 template <typename TA, int RM>
 cudaError_t launch_split(const AttnArgs& a, cudaStream_t st) {
     using L = AttnTile<TA>;
@@ -412,9 +711,12 @@ cudaError_t launch_split(const AttnArgs& a, cudaStream_t st) {
 template <typename TA>
 cudaError_t launch_attn_typed(const AttnArgs& a, cudaStream_t st) {
     const int R = a.Hq / a.Hkv;
-    // register sets for up to 2, 5 (the Nemotron-H layers) or 8 query heads per kv head
-    cudaError_t e = R <= 2 ? launch_split<TA, 2>(a, st) : R <= 5 ? launch_split<TA, 5>(a, st)
-                                                                 : launch_split<TA, 8>(a, st);
+    // bf16: the tensor-core walkers; fp32: register sets for up to 2, 5 (the
+    // Nemotron-H layers) or 8 query heads per kv head
+    cudaError_t e = attn_use_walk(a.S, a.Hkv, a.Tmax, sizeof(TA) == 2) ? launch_walk(a, st)
+                    : R <= 2        ? launch_split<TA, 2>(a, st)
+                    : R <= 5        ? launch_split<TA, 5>(a, st)
+                                    : launch_split<TA, 8>(a, st);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_combine_kernel<TA>, dim3(a.Hkv, a.S), dim3(R * (kAttnD / 2)), 0, st, a);
 }

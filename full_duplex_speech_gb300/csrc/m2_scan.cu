@@ -1005,24 +1005,6 @@ __global__ void __launch_bounds__(kComputeWarps == 16 ? 640 : kSsdThreads, 1) sc
     if (!compute) tc::tmem_dealloc(tm, kTmemCols);
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// The driver's tensor-map encoder, resolved once through the runtime.
-EncodeTiledFn encode_tiled() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
 // x viewed as a 3-D tensor [b][T][H*P] (innermost last; rows fx elements
 // apart, which is H*P for a dense x and wider for x inside the rows of a
 // projection output); a box is the
@@ -1030,7 +1012,7 @@ EncodeTiledFn encode_tiled() {
 // channels belong to the next head, or lie past the end and read as zero).
 template <typename TA, int P>
 cudaError_t make_x_map(const ScanArgs& a, CUtensorMap* map) {
-    EncodeTiledFn enc = encode_tiled();
+    tc::EncodeTiledFn enc = tc::encode_tiled();
     if (!enc) return cudaErrorNotSupported;
     const cuuint64_t HP = (cuuint64_t)a.s.H * P;
     const cuuint64_t dims[3] = {HP, (cuuint64_t)a.T, (cuuint64_t)a.batch};

@@ -4,6 +4,8 @@
 // memory matrix descriptors. Every wait here is bounded in time.
 #pragma once
 
+#include <cuda.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace m2 {
@@ -91,6 +93,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, 
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
         "[%5];" ::"r"(smem_u32(dst)),
         "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 2-D tiled TMA load of one box of `tmap` at element coordinates (x, y)
+// (innermost first). x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -216,6 +228,26 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t k, u
 // blocks of 8 at stride 128 B, K groups of 8 at stride (mn_extent/8)*128 B.
 __host__ __device__ __forceinline__ uint32_t mn_inter_off(uint32_t mn, uint32_t k, uint32_t mn_extent) {
     return (k >> 3) * (mn_extent >> 3) * 128u + (mn >> 3) * 128u + (k & 7u) * 16u + (mn & 7u) * 2u;
+}
+
+// ------------------------------------------------------------ host helpers
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, resolved once through the runtime (NULL if
+// the driver does not offer it).
+inline EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
 }
 
 }  // namespace tc

@@ -306,8 +306,12 @@ m2_status mamba2_linear_bf16(int rows, int in_features, int out_features, const 
  *   per kv head; n_kv_heads and n_sessions at most 65535; max_len >= 1.
  *   n_sessions == 0 is a no-op once the arguments check out.
  * Scratch: workspace of at least mamba2_attn_decode_workspace_bytes(...):
- *   per-chunk partial results (chunks of up to 128 positions in bf16, 64 in
- *   fp32; shorter where few sessions and kv heads would leave the GPU idle).
+ *   partial results over runs of positions (in bf16, runs of 64-position
+ *   chunks, enough runs per session and kv head to fill the GPU; in fp32,
+ *   chunks of up to 64 positions, shorter where few sessions and kv heads
+ *   would leave the GPU idle). bf16 products (scores, and the softmax weights
+ *   split into two bf16 terms times the values) run on the tensor cores with
+ *   fp32 accumulation.
  * Errors: M2_EINVAL (NULL pointer, non-positive size, non-finite scale),
  *   M2_ESHAPE, M2_EALIGN, M2_EWORKSPACE, M2_EUNSUPPORTED, M2_ECUDA. A length
  *   outside [0, max_len) is seen only on the device: that session's out is
