@@ -436,7 +436,8 @@ def lm_position_leg(m2, torch, dev, stream, peaks):
     out = {"sessions": S, "blocks": cfg.kinds, "cached_positions": cached, "us_per_position": us,
            "bytes_per_position": nbytes, "achieved_gbs": nbytes / (us * 1e-6) / 1e9,
            "frac_hbm": nbytes / (us * 1e-6) / 1e9 / peaks["hbm"],
-           "kernels_per_position": 4 * cfg.kinds.count("M") + 4 * cfg.kinds.count("*")}
+           # 'M': in_proj, conv, state update, out_proj; '*': q|k|v, attention, out projection
+           "kernels_per_position": 4 * cfg.kinds.count("M") + 3 * cfg.kinds.count("*")}
     del wdev, layers, model, ws
     torch.cuda.synchronize()
     return out

@@ -13,28 +13,31 @@
 // query heads of a kv head share each read), at 2 x 256 B per position and
 // kv head in bf16 against 4R flops per byte.
 //
-// Two kernels, both launched with programmatic dependent launch:
-//  1. a split kernel that computes partial results over runs of positions:
-//     - bf16 caches: attn_walk_kernel, on the tensor cores. One CTA per
-//       (walker, kv head, session): a walker takes a run of 64-position
-//       chunks, brought into shared memory by 2-D TMA copies through a
-//       3-stage ring; its four warps keep their own online softmax over 16
-//       positions of every chunk, with the scores (query heads x positions)
-//       and the weighted values (query heads x dims) as mma.sync products.
-//     - fp32 caches: attn_split_kernel, on the CUDA cores. One CTA per (chunk
-//       of up to 64 positions, kv head, session; shorter chunks where there
-//       would be too few CTAs to fill the GPU). Two bulk copies (the TMA
-//       engine) bring the chunk's cached keys and values into shared memory;
-//       then scores (8 lanes per position, 16 dims a lane, the R heads' dot
-//       products reduced over the 8 lanes, q held in fp32 registers), the
-//       chunk's softmax statistics in the log2 domain (m = max, l = sum of
-//       2^(a - m)) and acc = sum_t 2^(a_t - m) v_t (16 threads per value row,
-//       8 dims each, all R heads at once), written as the chunk's partial result.
-//     The run holding position len[s] takes the new key and value from the
-//     inputs instead of the cache, and writes them into the cache there (no
-//     other CTA reads that slot).
-//  2. attn_combine_kernel: per (kv head, session), merges the partial results:
-//     M = max_i m_i, out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.
+// Launched with programmatic dependent launch:
+//  - bf16 caches: attn_walk_kernel alone, on the tensor cores. One CTA
+//    ("walker") per (walker, kv head, session) takes a run of 64-position
+//    chunks, brought into shared memory by 2-D TMA copies through a 3-stage
+//    ring; its four warps keep their own online softmax over 16
+//    positions of every chunk, with the scores (query heads x positions) and
+//    the weighted values (query heads x dims) as mma.sync products. The
+//    walkers of one (session, kv head) form a thread-block cluster and merge
+//    their results through distributed shared memory:
+//        M = max_w m_w, out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w.
+//  - fp32 caches: two kernels.
+//    1. attn_split_kernel, on the CUDA cores. One CTA per (chunk of up to 64
+//       positions, kv head, session; shorter chunks where there would be too
+//       few CTAs to fill the GPU). Two bulk copies (the TMA engine) bring the
+//       chunk's cached keys and values into shared memory; then scores (8
+//       lanes per position, 16 dims a lane, the R heads' dot products reduced
+//       over the 8 lanes, q held in fp32 registers), the chunk's softmax
+//       statistics in the log2 domain (m = max, l = sum of 2^(a - m)) and
+//       acc = sum_t 2^(a_t - m) v_t (16 threads per value row, 8 dims each,
+//       all R heads at once), written as the chunk's partial result.
+//    2. attn_combine_kernel: per (kv head, session), merges the chunks'
+//       partial results with the same formula.
+// The run holding position len[s] takes the new key and value from the
+// inputs instead of the cache, and writes them into the cache there (no other
+// CTA reads that slot).
 #include "m2_common.cuh"
 #include "m2_launch.h"
 #include "m2_tc.cuh"
@@ -68,20 +71,17 @@ struct AttnTile {
 
 __host__ __device__ inline int attn_chunks(int Tmax, int tc) { return (Tmax + tc - 1) / tc; }
 
-// Positions per chunk: the most a CTA holds, halved (down to 32) while the
-// grid would have fewer than two CTAs per SM of the 152-SM GB300, so that a
-// short cache of few sessions still spreads over the GPU. A function of the
-// sizes alone: the workspace query needs no device.
-int attn_walk_chunks(int S, int Hkv, int Tmax);
-
 // bf16 caches go to the tensor-core walkers, whose 2-D copies address the
 // caches' rows (S x Hkv x Tmax of them) with 32-bit coordinates.
 bool attn_use_walk(int S, int Hkv, int Tmax, bool bf16) {
     return bf16 && (long long)S * Hkv * Tmax < (1LL << 31) - 64;
 }
 
+// Positions per chunk of the split kernel: the most a CTA holds, halved (down
+// to 32) while the grid would have fewer than two CTAs per SM of the 152-SM
+// GB300, so that a short cache of few sessions still spreads over the GPU. A
+// function of the sizes alone: the workspace query needs no device.
 int attn_chunk_len(int S, int Hkv, int Tmax, bool bf16) {
-    if (attn_use_walk(S, Hkv, Tmax, bf16)) return attn_walk_chunks(S, Hkv, Tmax) * 64;  // a walker's run of 64-position chunks
     int tc = bf16 ? AttnTile<bf16_t>::kTc : AttnTile<float>::kTc;
     while (tc > 32 && (long)S * Hkv * attn_chunks(Tmax, tc) < 2 * 152) tc /= 2;
     return tc;
@@ -409,26 +409,46 @@ __global__ void __launch_bounds__(kAttnMaxR * 64) attn_combine_kernel(AttnArgs a
 }
 
 // ---------------------------------------------------------------------------
-// bf16 caches: the split kernel on the tensor cores. A CTA ("walker") takes a
-// run of consecutive 64-position chunks of one (session, kv head); a 3-stage
-// ring of 2-D TMA copies (128-byte swizzle) keeps the next chunks' keys and
-// values in flight while it computes. Each of its four warps takes 16
-// positions of every chunk and keeps its own online softmax, so the warps
-// meet only at the chunk boundary where a stage is refilled:
-//     scores  S (16 x 16) = Q (16 query rows, R real) . K^T      mma m16n8k16
-//     P = 2^(S log2e scale - m), m the running max, l += sum P
-//     acc (16 x 128) += P . V      (P as bf16 hi + lo: two MMAs)
-// The scores' accumulator fragments are the P operand's fragments as they
-// stand (row = query head, column = position). The four warps' (m, l, acc)
-// are merged at the end into the walker's partial result, which the combine
-// kernel merges with the other walkers' as it does the chunks'.
-constexpr int kWalkTc = 64;                        // positions per chunk
+// bf16 caches on the tensor cores. A CTA ("walker") takes a run of
+// consecutive 64-position chunks of one (session, kv head); a ring of 2-D TMA
+// copies (128-byte swizzle) keeps the next chunks' keys and values in flight
+// while it computes. Each of its four warps takes 16 positions of every chunk
+// and keeps its own online softmax, so the warps meet only at the chunk
+// boundary where a stage is refilled:
+//     scores  S^T (16 positions x 8 heads, R real) = K . Q^T     mma m16n8k16
+//     P = 2^(S log2e scale - m), m the running max per head, l += sum P
+//     acc^T (128 dims x 8 heads) += V^T . P^T   (P as bf16 hi + lo: two MMAs)
+// Positions are the products' M (or K) side and the R <= 8 heads their N
+// side, so no MMA works on rows of zeros. The scores' accumulator fragments
+// become the B operand of the second product by an in-register transpose of
+// each 8 x 8 block (movmatrix). At the end the four warps' (m, l, acc) merge
+// into the walker's own in shared memory. The W walkers of
+// one (session, kv head) form one thread-block cluster: walker w owns query
+// heads w, w + W, ...; every walker stores its (m, l, acc) of each head into
+// the owner's shared memory (distributed shared memory), and after one
+// cluster barrier each owner merges what it received and writes out, so one
+// launch computes the whole decode position.
+constexpr int kWalkTc = 64;                   // positions per chunk
 constexpr int kWalkStages = 3;
 constexpr int kWalkThreads = 128;
-constexpr uint32_t kWalkBox = kWalkTc * 128;        // one box: 64 rows x 64 dims of bf16 (8 KiB)
-constexpr uint32_t kWalkStage = 4 * kWalkBox;       // K (2 boxes) + V (2 boxes)
-constexpr uint32_t kWalkBar = kWalkStages * kWalkStage;
-constexpr uint32_t kWalkSmem = kWalkBar + 64 + 1024;  // + barriers, + slack to align to 1024
+constexpr int kWalkMaxW = 16;                 // walkers per cluster, at most
+constexpr uint32_t kWalkBox = kWalkTc * 128;  // one box: 64 rows x 64 dims of bf16 (8 KiB)
+constexpr uint32_t kWalkStage = 4 * kWalkBox; // K (2 boxes) + V (2 boxes)
+// After the ring: the slots an owner receives, [head / W][walker], each a
+// walker's acc (128 floats relative to its max) then (max, sum); then the
+// ring's barriers.
+constexpr int kWalkSlots = kAttnMaxR + kWalkMaxW - 1;  // ceil(R / W) W, at most
+constexpr uint32_t kWalkSlotF = kAttnD + 2;
+constexpr uint32_t kWalkRecv = kWalkStages * kWalkStage;
+constexpr uint32_t kWalkBar = kWalkRecv + kWalkSlots * kWalkSlotF * 4;
+constexpr uint32_t kWalkSmem = kWalkBar + kWalkStages * 8 + 1024;  // + barriers, + slack to align to 1024
+static_assert(2 * (kWalkSmem + 1024) <= 228 * 1024, "two CTAs an SM");
+// The four warps' merge, over the first stage (no longer read): their
+// (m, l) and acc.
+constexpr uint32_t kWalkMl = 0;                                  // float [4][8][2]
+constexpr uint32_t kWalkAcc = kWalkMl + 4 * 8 * 2 * 4;           // float [4][8][128]
+static_assert(kWalkAcc + 4 * 8 * kAttnD * 4 <= kWalkStage, "the warps' merge fits in one stage");
+static_assert(kWalkThreads == kAttnD, "one thread per dim in the merge");
 
 // Byte offset of (row r, dim d) in a stage's K or V tile: two 64-dim boxes,
 // 128-byte rows, the 16-byte pieces of a row XOR-ed with r % 8.
@@ -447,13 +467,20 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
 }
-// d += A B, m16n8k16, bf16 in, fp32 accumulate; A's rows 8..15 are zero here
-__device__ __forceinline__ void mma_rows8(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+// d += A B, m16n8k16, bf16 in, fp32 accumulate
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// The warp's 8 x 8 matrix of 16-bit elements (lane l holding row l / 4,
+// columns 2 (l % 4) and + 1), transposed, in the same layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
@@ -461,25 +488,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
-__global__ void __launch_bounds__(kWalkThreads, 2) attn_walk_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmk,
-                                                                    const __grid_constant__ CUtensorMap tmv, int cpw) {
+// grid (W, Hkv, S), a cluster of W walkers per (session, kv head) when W > 1;
+// walker w takes chunks [w cpw, (w + 1) cpw) of those holding positions
+// 0 .. len. Two CTAs an SM.
+__global__ void __launch_bounds__(kWalkThreads, 2)
+    attn_walk_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     int cpw) {
     extern __shared__ uint8_t walk_smem_raw[];
     uint8_t* sm = walk_smem_raw + ((1024u - (tc::smem_u32(walk_smem_raw) & 1023u)) & 1023u);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kWalkBar);  // one per stage: its copies landed
-    const int wk = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+    const int W = gridDim.x, wk = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gq = lane >> 2, t = lane & 3;  // fragment row (query head) and lane in its quad
+    const int gq = lane >> 2, t = lane & 3;  // fragment row and lane in its quad
     const int R = a.Hq / a.Hkv;
     constexpr int RB = kAttnD * 2;  // bytes of one cached row
 
+    if (W > 1) tc::cluster_arrive_relaxed();  // waited on before the first remote store: every walker has started
+    const int row0 = (s * a.Hkv + g) * a.Tmax;  // tensor row of position 0
+    const int cb = wk * cpw;
     pdl_wait();  // the inputs and the caches may come from the previous kernel
     pdl_trigger();
     const int len = a.lens[s] + a.len_add;
-    if (len < 0 || len >= a.Tmax) return;  // refused; the combine kernel reports it
-    const int nch = len / kWalkTc + 1;     // chunks holding positions 0 .. len
-    const int cb = wk * cpw, ce = min(cb + cpw, nch);
-    if (cb >= ce) return;                  // past this session's positions
-    const int row0 = (s * a.Hkv + g) * a.Tmax;  // tensor row of position 0
+    const bool bad = len < 0 || len >= a.Tmax;  // the same for the whole cluster
+    const int nch = bad ? 0 : len / kWalkTc + 1;  // chunks holding positions 0 .. len
+    const int ce = min(cb + cpw, nch);           // empty past this session's positions
 
     auto issue = [&](int c) {  // one thread: chunk c's keys and values into its stage
         const int st = (c - cb) % kWalkStages;
@@ -496,37 +528,39 @@ __global__ void __launch_bounds__(kWalkThreads, 2) attn_walk_kernel(AttnArgs a, 
         tc::fence_mbar_init();
         for (int c = cb; c < min(ce, cb + kWalkStages); ++c) issue(c);
     }
-    // the query rows as the A operand (row = query head gq of this kv head;
-    // rows past R, and rows 8..15, zero): per 16-dim K-step two bf16 pairs
-    uint32_t qa[8][2];
+    // Q^T as the B operand (k = dims, n = query head gq of this kv head;
+    // heads past R zero): per 16-dim K-step two bf16 pairs
+    uint32_t qb[8][2];
     {
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(a.q) +
                                                                  (size_t)s * a.q_ss + (size_t)(g * R + min(gq, R - 1)) * kAttnD);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            qa[kk][0] = gq < R ? __ldg(qrow + 8 * kk + t) : 0u;
-            qa[kk][1] = gq < R ? __ldg(qrow + 8 * kk + 4 + t) : 0u;
+            qb[kk][0] = gq < R ? __ldg(qrow + 8 * kk + t) : 0u;
+            qb[kk][1] = gq < R ? __ldg(qrow + 8 * kk + 4 + t) : 0u;
         }
     }
     const float sl2 = a.scale * kLog2e;
-    float m = -1e30f, l = 0.f;  // running max (finite: a fully masked row stays harmless) and sum
-    float acc[16][4];
+    const bool h0ok = 2 * t < R, h1ok = 2 * t + 1 < R;  // this lane's heads 2t, 2t + 1
+    // per head 2t and 2t + 1: running max (finite: a fully masked head stays
+    // harmless), this lane's part of the sum, and acc^T (dims 16 dt + gq and
+    // + 8)
+    float m0 = -1e30f, m1 = -1e30f, l0 = 0.f, l1 = 0.f;
+    float acc[8][4];
 #pragma unroll
-    for (int dt = 0; dt < 16; ++dt)
+    for (int dt = 0; dt < 8; ++dt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[dt][e] = 0.f;
     __syncthreads();  // the barriers are initialised
 
-    bool ok = true;
+    bool ok = true;  // the same in every thread: the end-of-chunk barrier votes on it
     for (int c = cb; c < ce; ++c) {
         const int st = (c - cb) % kWalkStages;
         const uint32_t phase = ((c - cb) / kWalkStages) & 1;
         uint8_t* sK = sm + st * kWalkStage;
         uint8_t* sV = sK + 2 * kWalkBox;
-        if (!tc::mbar_wait(bar + st, phase)) {
-            atomicOr(a.err, ERR_MBAR_TIMEOUT_LOAD);
-            ok = false;
-        }
+        bool landed = tc::mbar_wait(bar + st, phase);
+        if (!landed) atomicOr(a.err, ERR_MBAR_TIMEOUT_LOAD);
         if (c == nch - 1) {
             // the chunk holding position len: the new key and value go into
             // their rows here and into the caches; the value rows past len
@@ -549,90 +583,118 @@ __global__ void __launch_bounds__(kWalkThreads, 2) attn_walk_kernel(AttnArgs a, 
             __syncthreads();
         }
         const uint32_t kb = tc::smem_u32(sK), vb = tc::smem_u32(sV);
-        // scores of this warp's positions 16 warp .. +15 (two 8-position tiles)
-        float sc[2][4];
+        // S^T of this warp's positions 16 warp .. + 15: the A operand from K
+        // (lanes 8j .. 8j + 7 address 8x8 piece j: positions + 8 (j & 1),
+        // dims + 8 (j >> 1)), two accumulation chains over the 8 K-steps
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int kr = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1), kc = 8 * (lane >> 4);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
-            const int r = 16 * warp + 8 * nt + (lane & 7);
-#pragma unroll
-            for (int kk2 = 0; kk2 < 4; ++kk2) {
-                uint32_t b[4];
-                ldsm_x4(kb + walk_off(r, 32 * kk2 + 8 * (lane >> 3)), b);
-                mma_rows8(sc[nt], qa[2 * kk2][0], qa[2 * kk2][1], b[0], b[1]);
-                mma_rows8(sc[nt], qa[2 * kk2 + 1][0], qa[2 * kk2 + 1][1], b[2], b[3]);
+            for (int kk = 0; kk < 8; kk += 2) {
+                uint32_t ka[4], kn[4];
+                ldsm_x4(kb + walk_off(kr, 16 * kk + kc), ka);
+                ldsm_x4(kb + walk_off(kr, 16 * kk + 16 + kc), kn);
+                mma16816(sa, ka, qb[kk][0], qb[kk][1]);
+                mma16816(sb, kn, qb[kk + 1][0], qb[kk + 1][1]);
             }
         }
-        // online softmax of row gq over these 16 positions (-inf past len)
-        float sv[2][2], mx = -INFINITY;
+        // online softmax per head over these 16 positions (-inf past len):
+        // this lane holds positions gq and gq + 8 of heads 2t and 2t + 1
+        const int pos = c * kWalkTc + 16 * warp + gq;
+        const bool p0ok = pos <= len, p1ok = pos + 8 <= len;
+        const float v00 = (p0ok && h0ok) ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+        const float v01 = (p0ok && h1ok) ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+        const float v10 = (p1ok && h0ok) ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+        const float v11 = (p1ok && h1ok) ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+        float mx0 = fmaxf(v00, v10), mx1 = fmaxf(v01, v11);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float c0 = ex2_approx(m0 - mn0), c1 = ex2_approx(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        const float p00 = ex2_approx(v00 - mn0), p01 = ex2_approx(v01 - mn1);  // 0 for -inf
+        const float p10 = ex2_approx(v10 - mn0), p11 = ex2_approx(v11 - mn1);
+        l0 = fmaf(l0, c0, p00 + p10);
+        l1 = fmaf(l1, c1, p01 + p11);
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int pos = c * kWalkTc + 16 * warp + 8 * nt + 2 * t + e;
-                sv[nt][e] = (pos <= len && gq < R) ? sc[nt][e] * sl2 : -INFINITY;
-                mx = fmaxf(mx, sv[nt][e]);
+        for (int dt = 0; dt < 8; ++dt) {
+            acc[dt][0] *= c0;
+            acc[dt][1] *= c1;
+            acc[dt][2] *= c0;
+            acc[dt][3] *= c1;
+        }
+        // P^T as the B operand (k = positions, n = head gq): bf16 hi + lo
+        // (p = hi + lo to ~2^-16), each 8x8 block of the accumulator layout
+        // transposed
+        const uint32_t ha = pack_bf16x2(p00, p01), hb = pack_bf16x2(p10, p11);
+        const uint32_t la = pack_bf16x2(p00 - __uint_as_float(ha << 16), p01 - __uint_as_float(ha & 0xFFFF0000u));
+        const uint32_t lb = pack_bf16x2(p10 - __uint_as_float(hb << 16), p11 - __uint_as_float(hb & 0xFFFF0000u));
+        const uint32_t bh0 = movmatrix_t(ha), bh1 = movmatrix_t(hb);
+        const uint32_t bl0 = movmatrix_t(la), bl1 = movmatrix_t(lb);
+        // acc^T += V^T P^T: the A operand V^T by transposed loads (piece j:
+        // positions + 8 (j >> 1), dims + 8 (j & 1)), 8 tiles of 16 dims
+        {
+            const int vr = 16 * warp + (lane & 7) + 8 * (lane >> 4), vc = 8 * ((lane >> 3) & 1);
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+                uint32_t va[4];
+                ldsm_x4_trans(vb + walk_off(vr, 16 * dt + vc), va);
+                mma16816(acc[dt], va, bh0, bh1);
+                mma16816(acc[dt], va, bl0, bl1);
             }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mn = fmaxf(m, mx);
-        const float corr = ex2_approx(m - mn);
-        m = mn;
-        float p[2][2];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) p[nt][e] = ex2_approx(sv[nt][e] - mn);  // 0 for -inf
-        l = fmaf(l, corr, (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]));
-#pragma unroll
-        for (int dt = 0; dt < 16; ++dt) {
-            acc[dt][0] *= corr;
-            acc[dt][1] *= corr;
         }
-        // P as bf16 hi + lo (p = hi + lo to ~2^-16): row gq, positions 2t, 2t+1 and 8+2t, 8+2t+1
-        const uint32_t h0 = pack_bf16x2(p[0][0], p[0][1]), h1 = pack_bf16x2(p[1][0], p[1][1]);
-        const uint32_t l0 = pack_bf16x2(p[0][0] - __uint_as_float(h0 << 16), p[0][1] - __uint_as_float(h0 & 0xFFFF0000u));
-        const uint32_t l1 = pack_bf16x2(p[1][0] - __uint_as_float(h1 << 16), p[1][1] - __uint_as_float(h1 & 0xFFFF0000u));
-        // acc += P V: 16 tiles of 8 dims, two per transposed 4-matrix load
-        const int vr = 16 * warp + 8 * ((lane >> 3) & 1) + (lane & 7);
-#pragma unroll
-        for (int dt2 = 0; dt2 < 8; ++dt2) {
-            uint32_t b[4];
-            ldsm_x4_trans(vb + walk_off(vr, 16 * dt2 + 8 * (lane >> 4)), b);
-            mma_rows8(acc[2 * dt2], h0, h1, b[0], b[1]);
-            mma_rows8(acc[2 * dt2], l0, l1, b[0], b[1]);
-            mma_rows8(acc[2 * dt2 + 1], h0, h1, b[2], b[3]);
-            mma_rows8(acc[2 * dt2 + 1], l0, l1, b[2], b[3]);
-        }
-        __syncthreads();  // every warp is done with this stage
-        if (tid == 0 && ok && c + kWalkStages < ce) issue(c + kWalkStages);
+        ok = __syncthreads_and(landed) != 0;  // every warp is done with this stage
+        if (!ok) break;
+        if (tid == 0 && c + kWalkStages < ce) issue(c + kWalkStages);
     }
     if (!ok) {
         // a copy did not land in time: let the copies still in flight land
-        // (bounded), leave no partial result (the combine kernel would read
-        // garbage: the error word is set)
+        // (bounded) and contribute nothing (the error word is set)
         if (tid == 0)
-            for (int i = 0; i < kWalkStages; ++i) tc::mbar_wait(bar + i, 0, 100000000ull), tc::mbar_wait(bar + i, 1, 100000000ull);
-        return;
-    }
-    // merge the four warps: the quad's sum of l, then (m, l, acc) through
-    // shared memory (over the stages, no longer read)
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    float* sml = reinterpret_cast<float*>(sm);                 // [4 warps][8 rows][2]
-    float* sacc = sml + 4 * 8 * 2;                             // [4 warps][8 rows][128]
-    if (t == 0) {
-        sml[(warp * 8 + gq) * 2] = m;
-        sml[(warp * 8 + gq) * 2 + 1] = l;
-    }
+            for (int i = 0; i < kWalkStages; ++i)
+                tc::mbar_wait(bar + i, 0, 100000000ull), tc::mbar_wait(bar + i, 1, 100000000ull);
+        m0 = m1 = -1e30f;
+        l0 = l1 = 0.f;
 #pragma unroll
-    for (int dt = 0; dt < 16; ++dt)
-        *reinterpret_cast<float2*>(sacc + (warp * 8 + gq) * kAttnD + 8 * dt + 2 * t) = make_float2(acc[dt][0], acc[dt][1]);
+        for (int dt = 0; dt < 8; ++dt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[dt][e] = 0.f;
+    }
+    __syncthreads();  // the stages are free for the merge
+    // the four warps: each head's sum over the warp's 8 lanes of it, then
+    // (m, l, acc) through shared memory
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    float* sml = reinterpret_cast<float*>(sm + kWalkMl);
+    float* sacc = reinterpret_cast<float*>(sm + kWalkAcc);
+    float* recv = reinterpret_cast<float*>(sm + kWalkRecv);
+    if (gq == 0) {
+        *reinterpret_cast<float2*>(sml + (warp * 8 + 2 * t) * 2) = make_float2(m0, l0);
+        *reinterpret_cast<float2*>(sml + (warp * 8 + 2 * t + 1) * 2) = make_float2(m1, l1);
+    }
+    {
+        float* a0 = sacc + (warp * 8 + 2 * t) * kAttnD + gq;  // head 2t, dim gq
+        float* a1 = a0 + kAttnD;                              // head 2t + 1
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) {
+            a0[16 * dt] = acc[dt][0];
+            a1[16 * dt] = acc[dt][1];
+            a0[16 * dt + 8] = acc[dt][2];
+            a1[16 * dt + 8] = acc[dt][3];
+        }
+    }
     __syncthreads();
-    const size_t part = ((size_t)s * a.Hkv + g) * attn_chunks(a.Tmax, cpw * kWalkTc) + wk;
-    float* wacc = a.ws + part * R * kAttnD;
-    float* wml = a.ws + (size_t)a.S * a.Hkv * attn_chunks(a.Tmax, cpw * kWalkTc) * R * kAttnD + part * R * 2;
+    if (W > 1) tc::cluster_wait();  // every walker of the cluster has started: its shared memory is there
+    // this walker's (max, sum, acc) per query head, acc relative to its max
+    // (a walker without positions: max -1e30, sum 0, acc 0), to the head's
+    // owner: slot (r / W) W + wk of walker r % W
     for (int r = 0; r < R; ++r) {
         float M = -1e30f;
 #pragma unroll
@@ -644,19 +706,56 @@ __global__ void __launch_bounds__(kWalkThreads, 2) attn_walk_kernel(AttnArgs a, 
             o = fmaf(f, sacc[(w * 8 + r) * kAttnD + tid], o);
             L = fmaf(f, sml[(w * 8 + r) * 2 + 1], L);
         }
-        wacc[r * kAttnD + tid] = o;
-        if (tid == 0) *reinterpret_cast<float2*>(wml + 2 * r) = make_float2(M, L);
+        if (W == 1) {
+            const float v = L > 0.f ? o / L : 0.f;  // a refused length (or a failed copy): zeros
+            reinterpret_cast<uint16_t*>(a.out)[(size_t)s * a.out_ss + (size_t)(g * R + r) * kAttnD + tid] =
+                float_to_bf16_bits(v);
+        } else {
+            const uint32_t slot = tc::smem_u32(recv + ((r / W) * W + wk) * kWalkSlotF);
+            const uint32_t owner = (uint32_t)(r % W);
+            tc::st_cluster_f32(tc::cluster_map(slot + 4u * tid, owner), o);
+            if (tid == 0) tc::st_cluster_f32x2(tc::cluster_map(slot + 4u * kAttnD, owner), make_float2(M, L));
+        }
+    }
+    if (bad && wk == 0 && g == 0 && tid == 0) atomicOr(a.err, ERR_ATTN_LENGTH);
+    if (W == 1) return;
+    tc::cluster_arrive();  // the stores into the owners' slots are visible ...
+    tc::cluster_wait();    // ... once every walker has made them
+    // out for the heads this walker owns: M = max_w m_w,
+    // out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w
+    for (int r = wk; r < R; r += W) {
+        const float* sl = recv + (r / W) * W * kWalkSlotF;
+        float M = -1e30f;
+        for (int w = 0; w < W; ++w) M = fmaxf(M, sl[w * kWalkSlotF + kAttnD]);
+        float o = 0.f, L = 0.f;
+        for (int w = 0; w < W; ++w) {
+            const float f = ex2_approx(sl[w * kWalkSlotF + kAttnD] - M);
+            o = fmaf(f, sl[w * kWalkSlotF + tid], o);
+            L = fmaf(f, sl[w * kWalkSlotF + kAttnD + 1], L);
+        }
+        const float v = L > 0.f ? o / L : 0.f;  // a refused length (or a failed copy): zeros
+        reinterpret_cast<uint16_t*>(a.out)[(size_t)s * a.out_ss + (size_t)(g * R + r) * kAttnD + tid] =
+            float_to_bf16_bits(v);
     }
 }
 
-// Chunks per walker for bf16 caches: enough walkers that sessions x kv heads
-// x walkers fill two CTAs an SM of the 152-SM GB300 (a function of the sizes
-// alone, like the workspace query that depends on it).
-int attn_walk_chunks(int S, int Hkv, int Tmax) {
+// Walkers per (session, kv head), a power of two, and 64-position chunks per
+// walker. The walkers double while the grid stays within two CTAs an SM of
+// the 152-SM GB300, every walker still gets a chunk, and the device runs one
+// cluster per (session, kv head) at once (`clusters[k]`: clusters of 2^k
+// walkers the device holds together, 0 where it runs none).
+struct WalkPlan {
+    int W, cpw;
+};
+WalkPlan walk_plan(int S, int Hkv, int Tmax, const int (&clusters)[5]) {
     const long nchunks = (Tmax + kWalkTc - 1) / kWalkTc;
     const long pairs = (long)S * Hkv;
-    const long walkers = pairs >= 2 * 152 ? 1 : (2 * 152 + pairs - 1) / pairs;
-    return (int)((nchunks + walkers - 1) / walkers);
+    int W = 1, k = 0;
+    while (k + 1 < 5 && pairs * 2 * W <= 2 * 152 && 2 * W <= nchunks && pairs <= clusters[k + 1]) W *= 2, ++k;
+    WalkPlan p;
+    p.W = W;
+    p.cpw = (int)((nchunks + W - 1) / W);
+    return p;
 }
 
 cudaError_t make_cache_map(const void* cache, const AttnArgs& a, CUtensorMap* map) {
@@ -672,23 +771,68 @@ cudaError_t make_cache_map(const void* cache, const AttnArgs& a, CUtensorMap* ma
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_walk(const AttnArgs& a, cudaStream_t st) {
+// Per device, once: the kernel's shared-memory and cluster-size attributes,
+// and how many clusters of 2, 4, 8 and 16 walkers the device holds at once.
+cudaError_t walk_setup(const int (**clusters)[5]) {
     static int configured_device = -1;
+    static int cached[5];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
         e = cudaFuncSetAttribute(attn_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWalkSmem);
         if (e != cudaSuccess) return e;
+        const bool wide = cudaFuncSetAttribute(attn_walk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                          cudaSuccess;
+        cached[0] = 1 << 30;
+        for (int k = 1; k < 5; ++k) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(1u << k, 1, 1);
+            cfg.blockDim = dim3(kWalkThreads);
+            cfg.dynamicSmemBytes = kWalkSmem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 1u << k;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if ((k == 4 && !wide) || cudaOccupancyMaxActiveClusters(&n, attn_walk_kernel, &cfg) != cudaSuccess) n = 0;
+            cached[k] = n;
+        }
+        (void)cudaGetLastError();  // a refused query leaves no sticky error
         configured_device = dev;
     }
+    *clusters = &cached;
+    return cudaSuccess;
+}
+
+cudaError_t launch_walk(const AttnArgs& a, cudaStream_t st) {
+    const int (*clusters)[5] = nullptr;
+    cudaError_t e = walk_setup(&clusters);
+    if (e != cudaSuccess) return e;
     CUtensorMap tmk, tmv;
     e = make_cache_map(a.k_cache, a, &tmk);
     if (e == cudaSuccess) e = make_cache_map(a.v_cache, a, &tmv);
     if (e != cudaSuccess) return e;
-    const int cpw = a.tc / kWalkTc;
-    const int nwalk = attn_chunks(a.Tmax, a.tc);
-    return launch_pdl(attn_walk_kernel, dim3(nwalk, a.Hkv, a.S), dim3(kWalkThreads), kWalkSmem, st, a, tmk, tmv, cpw);
+    const WalkPlan p = walk_plan(a.S, a.Hkv, a.Tmax, *clusters);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.W, a.Hkv, a.S);
+    cfg.blockDim = dim3(kWalkThreads);
+    cfg.dynamicSmemBytes = kWalkSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = p.W;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.W > 1 ? 2 : 1;
+    const int cpw = p.cpw;
+    return cudaLaunchKernelEx(&cfg, attn_walk_kernel, a, tmk, tmv, cpw);
 }
 
 template <typename TA, int RM>
@@ -708,15 +852,14 @@ cudaError_t launch_split(const AttnArgs& a, cudaStream_t st) {
     return launch_pdl(attn_split_kernel<TA, RM>, dim3(nch, a.Hkv, a.S), dim3(kAttnThreads), L::kBytes, st, a);
 }
 
+// fp32 caches (and bf16 caches past the walkers' 32-bit row coordinates): the
+// split kernel over chunks, then the combine kernel
 template <typename TA>
-cudaError_t launch_attn_typed(const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_split_combine(const AttnArgs& a, cudaStream_t st) {
     const int R = a.Hq / a.Hkv;
-    // bf16: the tensor-core walkers; fp32: register sets for up to 2, 5 (the
-    // Nemotron-H layers) or 8 query heads per kv head
-    cudaError_t e = attn_use_walk(a.S, a.Hkv, a.Tmax, sizeof(TA) == 2) ? launch_walk(a, st)
-                    : R <= 2        ? launch_split<TA, 2>(a, st)
-                    : R <= 5        ? launch_split<TA, 5>(a, st)
-                                    : launch_split<TA, 8>(a, st);
+    cudaError_t e = R <= 2   ? launch_split<TA, 2>(a, st)
+                    : R <= 5 ? launch_split<TA, 5>(a, st)
+                             : launch_split<TA, 8>(a, st);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_combine_kernel<TA>, dim3(a.Hkv, a.S), dim3(R * (kAttnD / 2)), 0, st, a);
 }
@@ -725,6 +868,7 @@ cudaError_t launch_attn_typed(const AttnArgs& a, cudaStream_t st) {
 
 size_t attn_workspace_bytes(int S, int Hq, int Hkv, int Tmax, bool bf16) {
     if (S <= 0 || Hq <= 0 || Hkv <= 0 || Tmax <= 0 || Hq % Hkv) return 0;
+    if (attn_use_walk(S, Hkv, Tmax, bf16)) return 0;  // the walkers merge in shared memory
     const int tc = attn_chunk_len(S, Hkv, Tmax, bf16);
     const size_t parts = (size_t)S * Hkv * attn_chunks(Tmax, tc) * (Hq / Hkv);
     return parts * (kAttnD + 2) * sizeof(float);
@@ -732,9 +876,10 @@ size_t attn_workspace_bytes(int S, int Hq, int Hkv, int Tmax, bool bf16) {
 
 cudaError_t launch_attn_decode(const AttnArgs& a0, cudaStream_t st) {
     if (a0.S == 0) return cudaSuccess;
+    if (attn_use_walk(a0.S, a0.Hkv, a0.Tmax, a0.bf16)) return launch_walk(a0, st);
     AttnArgs a = a0;
     a.tc = attn_chunk_len(a.S, a.Hkv, a.Tmax, a.bf16);
-    return a.bf16 ? launch_attn_typed<bf16_t>(a, st) : launch_attn_typed<float>(a, st);
+    return a.bf16 ? launch_split_combine<bf16_t>(a, st) : launch_split_combine<float>(a, st);
 }
 
 }  // namespace m2

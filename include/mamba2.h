@@ -305,25 +305,29 @@ m2_status mamba2_linear_bf16(int rows, int in_features, int out_features, const 
  * Sizes: head_dim 128; n_heads a multiple of n_kv_heads, at most 8 query heads
  *   per kv head; n_kv_heads and n_sessions at most 65535; max_len >= 1.
  *   n_sessions == 0 is a no-op once the arguments check out.
- * Scratch: workspace of at least mamba2_attn_decode_workspace_bytes(...):
- *   partial results over runs of positions (in bf16, runs of 64-position
- *   chunks, enough runs per session and kv head to fill the GPU; in fp32,
- *   chunks of up to 64 positions, shorter where few sessions and kv heads
- *   would leave the GPU idle). bf16 products (scores, and the softmax weights
- *   split into two bf16 terms times the values) run on the tensor cores with
- *   fp32 accumulation.
+ * Scratch: workspace of at least mamba2_attn_decode_workspace_bytes(...).
+ *   bf16 caches need none (workspace may be NULL with workspace_bytes 0):
+ *   one kernel, whose CTAs each take a run of 64-position chunks of one
+ *   (session, kv head) and, as one thread-block cluster per (session, kv
+ *   head), merge their partial results in shared memory. The products
+ *   (scores, and the softmax weights split into two bf16 terms times the
+ *   values) run on the tensor cores with fp32 accumulation. fp32 caches (and
+ *   bf16 caches of 2^31 rows or more) take two kernels: partial results per
+ *   chunk of up to 64 positions (shorter where few sessions and kv heads
+ *   would leave the GPU idle) in the workspace, then their merge.
  * Errors: M2_EINVAL (NULL pointer, non-positive size, non-finite scale),
  *   M2_ESHAPE, M2_EALIGN, M2_EWORKSPACE, M2_EUNSUPPORTED, M2_ECUDA. A length
  *   outside [0, max_len) is seen only on the device: that session's out is
  *   zero, its caches are untouched, and the device error word reads 0x104
- *   (mamba2_device_error). Two kernels, asynchronous on `stream`. */
+ *   (mamba2_device_error). Asynchronous on `stream`. */
 m2_status mamba2_attn_decode(int n_sessions, int n_heads, int n_kv_heads, int head_dim, int max_len, m2_dtype act,
                              const int32_t* lengths, const void* q, const void* k_new, const void* v_new,
                              void* k_cache, void* v_cache, float scale, void* out, void* workspace,
                              size_t workspace_bytes, void* stream);
 
 /* Bytes of device scratch that mamba2_attn_decode needs (0 if the sizes are
- * invalid or n_sessions is 0). */
+ * invalid, n_sessions is 0, or the caches are bf16 of fewer than 2^31 rows,
+ * n_sessions x n_kv_heads x max_len). */
 size_t mamba2_attn_decode_workspace_bytes(int n_sessions, int n_heads, int n_kv_heads, int head_dim, int max_len,
                                           m2_dtype act);
 

@@ -159,18 +159,21 @@ def test_attn_decode_validation_without_gpu(m2):
     assert call(ptrs=[lens, q, kn, vn, None, vc]) == 1
     assert call(ptrs=[lens + 2, q, kn, vn, kc, vc]) == 3    # lengths not 4-byte aligned
     assert call(ptrs=[lens, q + 8, kn, vn, kc, vc]) == 3    # q not 16-byte aligned
-    need = m2.mamba2_attn_decode_workspace_bytes(2, 40, 8, 128, 100)
-    # bf16: one partial result per walker; 16 (session, kv head) pairs over
-    # 100 positions (two 64-position chunks) get a walker per chunk
-    assert need == 2 * 8 * 2 * 5 * 130 * 4
-    # fp32: one per chunk; chunks shrink to 32 positions (4 a pair) so that
-    # the grid is not smaller than it must be
-    assert m2.mamba2_attn_decode_workspace_bytes(2, 40, 8, 128, 100, "f32") == 2 * 8 * 4 * 5 * 130 * 4
-    # 64 sessions over 750 positions: 512 pairs fill the GPU, one walker a pair
-    assert m2.mamba2_attn_decode_workspace_bytes(64, 40, 8, 128, 750) == 64 * 8 * 1 * 5 * 130 * 4
-    # one session over 7501 positions: 118 chunks over 30 walkers a kv head
-    assert m2.mamba2_attn_decode_workspace_bytes(1, 40, 8, 128, 7501) == 1 * 8 * 30 * 5 * 130 * 4
-    assert call(wsb=need - 1) == 6
+    # bf16: none; the walkers of a (session, kv head) merge in shared memory
+    assert m2.mamba2_attn_decode_workspace_bytes(2, 40, 8, 128, 100) == 0
+    assert m2.mamba2_attn_decode_workspace_bytes(64, 40, 8, 128, 750) == 0
+    assert m2.mamba2_attn_decode_workspace_bytes(1, 40, 8, 128, 7501) == 0
+    # fp32: one partial result per chunk; chunks shrink to 32 positions (4 a
+    # pair) so that the grid is not smaller than it must be
+    need = m2.mamba2_attn_decode_workspace_bytes(2, 40, 8, 128, 100, "f32")
+    assert need == 2 * 8 * 4 * 5 * 130 * 4
+    # 64 sessions over 750 positions: 64-position chunks fill the GPU
+    assert m2.mamba2_attn_decode_workspace_bytes(64, 40, 8, 128, 750, "f32") == 64 * 8 * 12 * 5 * 130 * 4
+    assert call(wsb=need - 1, act="f32") == 6
+    # bf16 takes no workspace at all: past the host checks (the device check
+    # is what stops it here, with no GPU)
+    assert m2.mamba2_attn_decode(2, 40, 8, 128, 100, "bf16", lens, q, kn, vn, kc, vc, 0.088, out, None,
+                                 workspace_bytes=0, stream=0, check=False) not in (1, 2, 3, 6)
     assert m2.mamba2_attn_decode_workspace_bytes(2, 40, 8, 64, 100) == 0
 
 

@@ -141,11 +141,12 @@ def test_attn_decode_consecutive_positions(m2):
     np.testing.assert_array_equal(from_dev_act(dev["v_cache"], "bf16"), vc)
 
 
-def test_attn_decode_refuses_a_length_past_the_cache(m2):
+@pytest.mark.parametrize("Tmax", [64, 300])
+def test_attn_decode_refuses_a_length_past_the_cache(m2, Tmax):
     """A length the host cannot see is checked on the device: that session
     gets zeros and untouched caches, the error word reads 0x104, and the
-    other sessions are computed as usual."""
-    Tmax = 64
+    other sessions are computed as usual (one walker per session and kv head
+    at 64 positions; a cluster of 4 walkers at 300)."""
     m2.mamba2_device_error(None)  # start from a clear error word
     inp = attn_inputs(307, 2, HQ, HKV, D, Tmax, [10, Tmax], "bf16")
     out, dev = _run(m2, inp, HQ, HKV, Tmax, 0.1)
