@@ -62,13 +62,22 @@ __device__ __forceinline__ float pair_fma(uint32_t p, uint32_t xp, float acc) {
     return acc;
 }
 
+// (v & 0x000F000F) | hi, one three-input logic operation: hi (the bf16 pair
+// 0x4300 0x4300) is passed in a register so that the mask can be the one
+// immediate operand
+__device__ __forceinline__ uint32_t nib_pair(uint32_t v, uint32_t hi) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(r) : "r"(v), "r"(hi));
+    return r;
+}
+
 // sum over the 8 inputs of one word of (128 + q) * x; xw holds the word's x
 // as the pairs (x_k, x_{k+4}), k = 0..3, matching the weight pairs
-__device__ __forceinline__ float word_dot(uint32_t w, const uint4& xw, float acc) {
-    acc = pair_fma((w & 0x000F000Fu) | 0x43004300u, xw.x, acc);
-    acc = pair_fma(((w >> 4) & 0x000F000Fu) | 0x43004300u, xw.y, acc);
-    acc = pair_fma(((w >> 8) & 0x000F000Fu) | 0x43004300u, xw.z, acc);
-    acc = pair_fma(((w >> 12) & 0x000F000Fu) | 0x43004300u, xw.w, acc);
+__device__ __forceinline__ float word_dot(uint32_t w, const uint4& xw, uint32_t hi, float acc) {
+    acc = pair_fma(nib_pair(w, hi), xw.x, acc);
+    acc = pair_fma(nib_pair(w >> 4, hi), xw.y, acc);
+    acc = pair_fma(nib_pair(w >> 8, hi), xw.z, acc);
+    acc = pair_fma(nib_pair(w >> 12, hi), xw.w, acc);
     return acc;
 }
 
@@ -101,6 +110,9 @@ __global__ void __launch_bounds__(kQlThreads, 1) qlinear_kernel(QLinearArgs a) {
     const int gwarp = blockIdx.x * kQlWarps + warp, nwarps = gridDim.x * kQlWarps;
     uint16_t* yb = reinterpret_cast<uint16_t*>(a.y);
     const uint16_t* rb = reinterpret_cast<const uint16_t*>(a.residual);
+    // the bf16 pair (128, 128), kept in a register (not folded into an immediate)
+    uint32_t hi;
+    asm volatile("mov.b32 %0, 0x43004300;" : "=r"(hi));
 
     pdl_wait();  // x (and z, the residual) may come from the previous kernel
     for (int r0 = 0; r0 < a.rows; r0 += NB) {
@@ -134,21 +146,11 @@ __global__ void __launch_bounds__(kQlThreads, 1) qlinear_kernel(QLinearArgs a) {
         // the current item is computed, so a batch is always in flight.
         const int nbatch = (nchunks + kInFlight * 32 - 1) / (kInFlight * 32);
         int o = gwarp, bi = 0;
-        uint4 w[kInFlight];
-        uint32_t sb[kInFlight];
-        if (o < a.out) load_batch(a, o, bi, nchunks, ngroups, lane, w, sb);
         float acc[NB];
 #pragma unroll
         for (int r = 0; r < NB; ++r) acc[r] = 0.f;
-        while (o < a.out) {
-            int on = o, bn = bi + 1;
-            if (bn == nbatch) {
-                bn = 0;
-                on = o + nwarps;
-            }
-            uint4 wn[kInFlight];
-            uint32_t sbn[kInFlight];
-            if (on < a.out) load_batch(a, on, bn, nchunks, ngroups, lane, wn, sbn);
+        // one item: the batch in (w, sb) of row o; finishes the row at its last batch
+        auto compute = [&](const uint4 (&w)[kInFlight], const uint32_t (&sb)[kInFlight], int o, int bi) {
 #pragma unroll
             for (int k = 0; k < kInFlight; ++k) {
                 const int c = bi * kInFlight * 32 + lane + k * 32;
@@ -158,10 +160,10 @@ __global__ void __launch_bounds__(kQlThreads, 1) qlinear_kernel(QLinearArgs a) {
 #pragma unroll
                     for (int r = 0; r < NB; ++r) {
                         const uint4* xr = reinterpret_cast<const uint4*>(sx + ((size_t)r * nchunks + c) * kChunkPitch);
-                        float d0 = word_dot(w[k].x, xr[0], 0.f);
-                        float d1 = word_dot(w[k].y, xr[1], 0.f);
-                        d0 = word_dot(w[k].z, xr[2], d0);
-                        d1 = word_dot(w[k].w, xr[3], d1);
+                        float d0 = word_dot(w[k].x, xr[0], hi, 0.f);
+                        float d1 = word_dot(w[k].y, xr[1], hi, 0.f);
+                        d0 = word_dot(w[k].z, xr[2], hi, d0);
+                        d1 = word_dot(w[k].w, xr[3], hi, d1);
                         acc[r] = fmaf(scale, d0 + d1, fmaf(corr, ssum[r * nchunks + c], acc[r]));
                     }
                 }
@@ -186,13 +188,33 @@ __global__ void __launch_bounds__(kQlThreads, 1) qlinear_kernel(QLinearArgs a) {
 #pragma unroll
                 for (int r = 0; r < NB; ++r) acc[r] = 0.f;
             }
+        };
+        auto advance = [&](int& o, int& bi) {
+            if (++bi == nbatch) {
+                bi = 0;
+                o += nwarps;
+            }
+        };
+        // two register sets in turn: the next item's loads go into one while
+        // the other is computed (no copies between them)
+        uint4 wa[kInFlight], wb[kInFlight];
+        uint32_t sa[kInFlight], sbb[kInFlight];
+        if (o < a.out) load_batch(a, o, bi, nchunks, ngroups, lane, wa, sa);
+        while (o < a.out) {
+            int on = o, bn = bi;
+            advance(on, bn);
+            if (on < a.out) load_batch(a, on, bn, nchunks, ngroups, lane, wb, sbb);
+            compute(wa, sa, o, bi);
             o = on;
             bi = bn;
-#pragma unroll
-            for (int k = 0; k < kInFlight; ++k) {
-                w[k] = wn[k];
-                sb[k] = sbn[k];
-            }
+            if (o >= a.out) break;
+            on = o;
+            bn = bi;
+            advance(on, bn);
+            if (on < a.out) load_batch(a, on, bn, nchunks, ngroups, lane, wa, sa);
+            compute(wb, sbb, o, bi);
+            o = on;
+            bi = bn;
         }
         __syncthreads();  // x of this pass is consumed before the next is staged
     }
