@@ -10,7 +10,8 @@
 // (optionally normalised, m2_rowprep.cuh) in shared memory as bf16; each warp
 // streams whole weight rows with 16-byte loads (a lane takes 8 inputs at a
 // time, consecutive lanes consecutive 16-byte pieces, the next batch in
-// flight while the current one is computed), multiplies with mixed-precision
+// flight while the current one is computed, the two batches in two register
+// sets taken in turn), multiplies with mixed-precision
 // fmas (bf16 x bf16 products, exact in fp32) and reduces across the warp.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -98,19 +99,11 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_bf16_kernel(LinearArgs 
 
         const int nbatch = (npieces + kInFlight * 32 - 1) / (kInFlight * 32);
         int o = gwarp, bi = 0;
-        uint4 w[kInFlight];
-        if (o < a.out) load_batch(a, o, bi, npieces, lane, w);
         float acc[NB];
 #pragma unroll
         for (int r = 0; r < NB; ++r) acc[r] = 0.f;
-        while (o < a.out) {
-            int on = o, bn = bi + 1;
-            if (bn == nbatch) {
-                bn = 0;
-                on = o + nwarps;
-            }
-            uint4 wn[kInFlight];
-            if (on < a.out) load_batch(a, on, bn, npieces, lane, wn);
+        // one item: the batch in w of row o; finishes the row at its last batch
+        auto compute = [&](const uint4 (&w)[kInFlight], int o, int bi) {
 #pragma unroll
             for (int k = 0; k < kInFlight; ++k) {
                 const int c = bi * kInFlight * 32 + lane + k * 32;
@@ -138,10 +131,32 @@ __global__ void __launch_bounds__(kLinThreads, 1) linear_bf16_kernel(LinearArgs 
 #pragma unroll
                 for (int r = 0; r < NB; ++r) acc[r] = 0.f;
             }
+        };
+        auto advance = [&](int& o, int& bi) {
+            if (++bi == nbatch) {
+                bi = 0;
+                o += nwarps;
+            }
+        };
+        // two register sets in turn: the next item's loads go into one while
+        // the other is computed (no copies between them)
+        uint4 wa[kInFlight], wb[kInFlight];
+        if (o < a.out) load_batch(a, o, bi, npieces, lane, wa);
+        while (o < a.out) {
+            int on = o, bn = bi;
+            advance(on, bn);
+            if (on < a.out) load_batch(a, on, bn, npieces, lane, wb);
+            compute(wa, o, bi);
             o = on;
             bi = bn;
-#pragma unroll
-            for (int k = 0; k < kInFlight; ++k) w[k] = wn[k];
+            if (o >= a.out) break;
+            on = o;
+            bn = bi;
+            advance(on, bn);
+            if (on < a.out) load_batch(a, on, bn, npieces, lane, wa);
+            compute(wb, o, bi);
+            o = on;
+            bi = bn;
         }
         __syncthreads();  // x of this pass is consumed before the next is staged
     }
