@@ -100,6 +100,10 @@ __device__ __forceinline__ void bc_store_row(uint8_t* tiles, int row, int n0, in
 
 template <typename TA>
 __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nchunks) {
+    // the conv weights and bias of the CTA's 32 columns of 8 channels, read
+    // from global memory by its first warp only: the 24 CTAs of a group and
+    // the 8 warps of each would otherwise ask L2 for the same lines at once
+    __shared__ float4 sW[32][10];
     const Shape& s = a.s;
     const int c = blockIdx.x / kBcParts, part = blockIdx.x % kBcParts, g = blockIdx.y, b = blockIdx.z;
     const int T = a.T, Q = a.chunk;
@@ -120,13 +124,19 @@ __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nch
     const int L = min(Q, seq_len(a, b) - c0);  // rows of this chunk in the sequence
     if (L <= 0) return;                        // past the sequence end: no tile is read
 
-    // pre-conv rows r0-3 .. r0+kBcRows-1, weights and bias: every load is
-    // issued before any use, so all are in flight together. A row outside the
-    // sequence (and not in the initial tail) reads the chunk's first row, a
-    // valid address, and counts as zero.
+    // pre-conv rows r0-3 .. r0+kBcRows-1, and (first warp) the weights and
+    // bias: every load is issued before any use, so all are in flight
+    // together. A row outside the sequence (and not in the initial tail) reads
+    // the chunk's first row, a valid address, and counts as zero.
     Act8<TA> v[kBcRows + 3];
     bool have[kBcRows + 3];
     float4 w[8], b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
+    if (rs == 0 && real) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sW[cc][j] = ldg_pinned_f4(reinterpret_cast<const float4*>(a.conv_w) + ch0 + j);
+        sW[cc][8] = ldg_pinned_f4(reinterpret_cast<const float4*>(a.conv_b + ch0));
+        sW[cc][9] = ldg_pinned_f4(reinterpret_cast<const float4*>(a.conv_b + ch0) + 1);
+    }
     const bool any = real && r0 < L;
     if (any) {
 #pragma unroll
@@ -140,10 +150,13 @@ __global__ void __launch_bounds__(kBcThreads) scan_bc_kernel(ScanArgs a, int nch
                                           : ((size_t)b * T + (in_seq ? t : c0)) * a.fbc + (size_t)g * s.N + n0;
             v[k].load_pinned(base, elem);
         }
+    }
+    __syncthreads();
+    if (any) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = ldg_pinned_f4(reinterpret_cast<const float4*>(a.conv_w) + ch0 + j);
-        b0 = ldg_pinned_f4(reinterpret_cast<const float4*>(a.conv_b + ch0));
-        b1 = ldg_pinned_f4(reinterpret_cast<const float4*>(a.conv_b + ch0) + 1);
+        for (int j = 0; j < 8; ++j) w[j] = sW[cc][j];
+        b0 = sW[cc][8];
+        b1 = sW[cc][9];
     }
 #pragma unroll
     for (int r = 0; r < kBcRows; ++r) {
