@@ -60,7 +60,7 @@ WORKLOAD = ("Nemotron-H Mamba2 mixer, real shape H=128 P=80 N=128 G=8 K=4, batch
 # launch of this workload, from an ncu capture of the kernel. It describes one
 # version of the kernel source; for any other version the traffic is reported
 # as unknown (null).
-SSD_TRAFFIC = {"bytes": 8868096, "m2_scan_cu_sha1": "20a1b7c13aeb939fc60222be6552a25f432441de"}
+SSD_TRAFFIC = {"bytes": 8868096, "m2_scan_cu_sha1": "f2e8ceba94155ffc9651c1b51785356cc27d0f6a"}
 SCAN_BYTES_PER_TOKEN = 45312
 STATE_BYTES = 128 * 80 * 128 * 4
 TAIL_BYTES = 3 * 12288 * 2
