@@ -108,6 +108,22 @@ def test_attn_decode_longest_cache(m2):
     _check(out, ref, "bf16")
 
 
+@pytest.mark.parametrize("Hq,Hkv,Tmax,length", [
+    (40, 8, 750, 749),    # one session at 60 s: clusters of 8 walkers, 2 chunks each
+    (16, 2, 2000, 1999),  # 8 query heads per kv head, clusters of 16 walkers: every walker owns a head
+    (40, 8, 1500, 700),   # a length well inside the cache: the walkers past it hold no positions
+])
+def test_attn_decode_one_session_clusters(m2, Hq, Hkv, Tmax, length):
+    """One session, where the walkers of a kv head form a thread-block cluster
+    and merge through distributed shared memory."""
+    inp = attn_inputs(308, 1, Hq, Hkv, D, Tmax, [length], "bf16")
+    scale = 1.0 / math.sqrt(D)
+    out, dev = _run(m2, inp, Hq, Hkv, Tmax, scale)
+    ref, _, _ = _oracle(inp, scale)
+    _check(out, ref, "bf16")
+    np.testing.assert_array_equal(bits_of(dev["k_cache"]), _expected_cache_bits(inp["k_cache"], inp["k_new"], [length]))
+
+
 def test_attn_decode_many_sessions(m2):
     """64 sessions with lengths drawn in [0, 750) (60 s of frames)."""
     S, Tmax = 64, 750
