@@ -505,6 +505,11 @@ def run_gpu(args, world, rank, local):
     t_wall0 = time.time()
     torch.cuda.nvtx.range_push("bench_timed")
     with torch.cuda.stream(stream):
+        # ~1 ms of GPU spin ahead of the first event, so that the host has
+        # submitted the graph replays by the time the GPU reaches it: the
+        # timed region then holds the K steps' device time only, not the
+        # host's submission latency (which a short --steps run would feel)
+        torch.cuda._sleep(2_000_000)
         e0.record(stream)
         for _ in range(K // sweep):
             g_full.replay()
