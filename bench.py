@@ -438,7 +438,27 @@ def lm_position_leg(m2, torch, dev, stream, peaks):
            "frac_hbm": nbytes / (us * 1e-6) / 1e9 / peaks["hbm"],
            # 'M': in_proj, conv, state update, out_proj; '*': q|k|v, attention, out projection
            "kernels_per_position": 4 * cfg.kinds.count("M") + 3 * cfg.kinds.count("*")}
-    del wdev, layers, model, ws
+
+    # the full-history recompute of 300 positions through the same blocks
+    # (mamba2_lm_prefill from empty caches: chunked scans, the projections as
+    # GEMMs, attention position by position); each replay first restores the
+    # residual stream the call updates in place (a 2.7 MB copy, included)
+    T, chunk = 300, 128
+    pws = torch.empty(m2.mamba2_lm_workspace_bytes(model, S, T, chunk), dtype=torch.uint8, device=dev)
+    plens = torch.zeros((S,), dtype=torch.int32, device=dev)
+    h0 = torch.randn((S * T, cfg.hidden), device=dev).to(torch.bfloat16)
+    hp = torch.empty_like(h0)
+    torch.cuda.synchronize()
+
+    def prefill():
+        hp.copy_(h0)
+        m2.mamba2_lm_prefill(model, S, T, hp, plens, chunk, pws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        p_us = _time_graph(torch, stream, prefill, reps=3)
+    out["prefill_T300"] = {"positions": T, "chunk": chunk, "us_per_prefill": p_us,
+                           "positions_per_s": S * T / (p_us * 1e-6)}
+    del wdev, layers, model, ws, pws
     torch.cuda.synchronize()
     return out
 
@@ -628,7 +648,8 @@ def run_gpu(args, world, rank, local):
 
     # 4-bit group-64 quantized mixer projections (in_proj 4480 -> 22656,
     # out_proj 10240 -> 4480) for 1 and 4 rows of x (one cached frame of 1 or 4
-    # sessions), 4 random weight sets per shape (> L2) cycled in a graph
+    # sessions), and for 300 rows (a prefill of 300 positions: the tensor-core
+    # GEMM), 4 random weight sets per shape (> L2) cycled in a graph
     qlinear = {}
     torch.cuda.nvtx.range_push("qlinear")
     for name, n_in, n_out in (("in_proj", 4480, 22656), ("out_proj", 10240, 4480)):
@@ -638,7 +659,7 @@ def run_gpu(args, world, rank, local):
                           (torch.rand(n_out, n_in // 64, device=dev) * 0.01).bfloat16(),
                           (torch.rand(n_out, n_in // 64, device=dev) * -0.05).bfloat16()))
         wbytes = n_out * n_in // 2 + 2 * n_out * (n_in // 64) * 2
-        for rows in (1, 4):
+        for rows in (1, 4, 300):
             qx = torch.randn(rows, n_in, device=dev).bfloat16()
             qy = torch.empty(rows, n_out, dtype=torch.bfloat16, device=dev)
             torch.cuda.synchronize()
@@ -652,6 +673,9 @@ def run_gpu(args, world, rank, local):
             qlinear[f"{name}_rows{rows}"] = {"in": n_in, "out": n_out, "rows": rows, "us_per_call": q_us,
                                              "bytes_per_call": qb, "achieved_gbs": qb / (q_us * 1e-6) / 1e9,
                                              "frac_hbm": qb / (q_us * 1e-6) / 1e9 / peaks["hbm"]}
+            if rows >= 40:  # the GEMM: its tensor fraction (2 flops per weight and row)
+                tfs = 2.0 * rows * n_in * n_out / (q_us * 1e-6) / 1e12
+                qlinear[f"{name}_rows{rows}"].update({"tflops": tfs, "frac_bf16": tfs / peaks["bf16"]})
         del wsets
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()

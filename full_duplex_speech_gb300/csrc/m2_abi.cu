@@ -207,6 +207,7 @@ m2_status mamba2_qlinear_fused(int rows, int in_features, int out_features, int 
     a.biases = static_cast<const uint16_t*>(biases);
     a.residual = residual;
     a.y = y;
+    a.err = m2::device_error_word();
     cudaError_t e = m2::launch_qlinear(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? M2_OK : cuda_fail(e);
 }

@@ -97,10 +97,23 @@ struct QLinearArgs {
     const uint16_t* biases;   // [out, in/64] bf16
     const void* residual;     // NULL, or [rows, out] bf16 added before the rounding (may alias y)
     void* y;                  // [rows, out] bf16
+    unsigned int* err;        // device error word
 };
 // Rows of x the kernel takes per pass over the weights (0: `in` too large).
 int qlinear_rows_per_pass(int in);
 cudaError_t launch_qlinear(const QLinearArgs& a, cudaStream_t st);
+// The same layer as a tensor-core GEMM over tiles of 128 rows of x (no row
+// norm; x 16-byte aligned with rows a multiple of 16 bytes apart).
+cudaError_t launch_qgemm(const QLinearArgs& a, cudaStream_t st);
+// out[r] = row r of x normalised (RowNorm kind 1 or 2) and rounded to bf16,
+// bit for bit as the fused linear layers stage it; out is [rows, in].
+cudaError_t launch_row_norm(const RowNorm& nm, const void* x, long x_stride, int rows, int in, void* out,
+                            cudaStream_t st);
+// Rows of x from which launch_qlinear takes the GEMM (when no norm is fused):
+// measured, the decode kernel's passes of four rows cost more from about 20
+// rows (in_proj's shape) to 36 (out_proj's, whose 70 output tiles fill half
+// the SMs).
+constexpr int kQgemmMinRows = 40;
 
 // Dense bf16 linear layer for the few rows of a decode step: y = x W^T (+ residual).
 constexpr int kLinMaxIn = 16384;

@@ -24,7 +24,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Plan {
     long HP, GN, W, CH;          // mixer widths; W = in_proj output row
     long QKV, AO;                // attention row widths
-    size_t proj, y, mix, qkv, ao, attn;  // workspace parts (bytes, aligned)
+    size_t proj, y, mix, qkv, ao, attn, xn;  // workspace parts (bytes, aligned)
     size_t total;
 };
 
@@ -67,7 +67,12 @@ m2_status plan(const m2_lm* m, int S, int T, int chunk, bool cached, Plan* p) {
     p->attn = any_attn ? up(mamba2_attn_decode_workspace_bytes(S, m->n_heads, m->n_kv_heads, m->head_dim,
                                                                 m->max_len, M2_BF16))
                        : 0;
-    p->total = p->proj + p->y + p->mix + p->qkv + p->ao + p->attn;
+    // a recompute of many rows normalises the projections' input rows into
+    // their own buffer, so that the 4-bit projections run as GEMMs
+    p->xn = (!cached && rows >= (size_t)m2::kQgemmMinRows)
+                ? up(rows * (size_t)(m->hidden > p->HP ? m->hidden : p->HP) * 2)
+                : 0;
+    p->total = p->proj + p->y + p->mix + p->qkv + p->ao + p->attn + p->xn;
     return M2_OK;
 }
 
@@ -119,7 +124,14 @@ m2_status run(const m2_lm* m, int S, int T, void* hidden, const int32_t* lengths
     uint16_t* qkv = reinterpret_cast<uint16_t*>(ws + p.proj + p.y + p.mix);
     uint16_t* ao = reinterpret_cast<uint16_t*>(ws + p.proj + p.y + p.mix + p.qkv);
     float* attn_ws = reinterpret_cast<float*>(ws + p.proj + p.y + p.mix + p.qkv + p.ao);
+    uint16_t* xn = p.xn ? reinterpret_cast<uint16_t*>(ws + p.proj + p.y + p.mix + p.qkv + p.ao + p.attn) : nullptr;
     const int rows = S * T;
+    auto row_norm = [&](const m2::RowNorm& nm, const void* x, long x_stride, int in) -> m2_status {
+        cudaError_t e = m2::launch_row_norm(nm, x, x_stride, rows, in, xn, static_cast<cudaStream_t>(stream));
+        if (e == cudaSuccess) return M2_OK;
+        m2::record_cuda_error(e);
+        return M2_ECUDA;
+    };
     const m2_dims& md = m->mixer;
     const long HP = p.HP, GN = p.GN, W = p.W;
 
@@ -127,9 +139,17 @@ m2_status run(const m2_lm* m, int S, int T, void* hidden, const int32_t* lengths
         const m2_lm_layer& L = m->layers[l];
         m2_row_norm pre{M2_NORM_RMS, L.norm_w, m->norm_eps, 1, nullptr, 0};
         if (m->kinds[l] == 'M') {
-            // proj = in_proj(RMSNorm(h)): rows of z | x | B | C | dt
-            st = mamba2_qlinear_fused(rows, m->hidden, (int)W, 64, 4, hidden, m->hidden, &pre, L.in_wq, L.in_scales,
-                                      L.in_biases, nullptr, proj, stream);
+            // proj = in_proj(RMSNorm(h)): rows of z | x | B | C | dt (for many
+            // rows: the norm into xn, then the projection as a GEMM)
+            if (xn) {
+                st = row_norm(m2::RowNorm{1, L.norm_w, m->norm_eps, 1, nullptr, 0}, hidden, m->hidden, m->hidden);
+                if (st == M2_OK)
+                    st = mamba2_qlinear_fused(rows, m->hidden, (int)W, 64, 4, xn, m->hidden, nullptr, L.in_wq,
+                                              L.in_scales, L.in_biases, nullptr, proj, stream);
+            } else {
+                st = mamba2_qlinear_fused(rows, m->hidden, (int)W, 64, 4, hidden, m->hidden, &pre, L.in_wq,
+                                          L.in_scales, L.in_biases, nullptr, proj, stream);
+            }
             if (st != M2_OK) return st;
             const uint16_t* x = proj + HP;
             const uint16_t* B = x + HP;
@@ -147,9 +167,16 @@ m2_status run(const m2_lm* m, int S, int T, void* hidden, const int32_t* lengths
                                               stream);
             if (st != M2_OK) return st;
             // h = h + out_proj(gated_norm(y, z))
-            m2_row_norm gated{M2_NORM_GATED, L.gnorm_w, m->norm_eps, md.ngroups, proj, W};
-            st = mamba2_qlinear_fused(rows, (int)HP, m->hidden, 64, 4, y, HP, &gated, L.out_wq, L.out_scales,
-                                      L.out_biases, hidden, hidden, stream);
+            if (xn) {
+                st = row_norm(m2::RowNorm{2, L.gnorm_w, m->norm_eps, md.ngroups, proj, W}, y, HP, (int)HP);
+                if (st == M2_OK)
+                    st = mamba2_qlinear_fused(rows, (int)HP, m->hidden, 64, 4, xn, HP, nullptr, L.out_wq,
+                                              L.out_scales, L.out_biases, hidden, hidden, stream);
+            } else {
+                m2_row_norm gated{M2_NORM_GATED, L.gnorm_w, m->norm_eps, md.ngroups, proj, W};
+                st = mamba2_qlinear_fused(rows, (int)HP, m->hidden, 64, 4, y, HP, &gated, L.out_wq, L.out_scales,
+                                          L.out_biases, hidden, hidden, stream);
+            }
             if (st != M2_OK) return st;
         } else {
             // q | k | v = Wqkv RMSNorm(h)

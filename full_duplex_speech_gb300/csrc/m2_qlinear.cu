@@ -257,7 +257,37 @@ cudaError_t launch_nb(const QLinearArgs& a, cudaStream_t st) {
     }
 }
 
+// One row of x normalised as the fused layers stage it (the same code, so the
+// same bf16 bits), written out: the input of the GEMM for many rows.
+template <int KIND>
+__global__ void __launch_bounds__(256) row_norm_kernel(RowNorm nm, const void* x, long x_stride, int in, void* out) {
+    __shared__ float scratch[kQlMaxIn / rowprep::kChunk];
+    __shared__ float srs[kMaxNormGroups];
+    const int r = blockIdx.x;
+    pdl_wait();  // x (and the gate) may come from the previous kernel
+    pdl_trigger();
+    rowprep::norm_scales<256, KIND>(x, x_stride, nm, in, r, 1, 1, scratch, srs);
+    for (int c = threadIdx.x; c < in / rowprep::kChunk; c += 256) {
+        uint32_t wd[16];
+        rowprep::staged32<KIND>(x, x_stride, nm, in, r, 0, 1, c * rowprep::kChunk, srs, wd);
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + (size_t)r * in + c * rowprep::kChunk);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(wd[4 * k], wd[4 * k + 1], wd[4 * k + 2], wd[4 * k + 3]);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_row_norm(const RowNorm& nm, const void* x, long x_stride, int rows, int in, void* out,
+                            cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    if (in > kQlMaxIn || in % rowprep::kChunk != 0) return cudaErrorInvalidValue;
+    switch (nm.kind) {
+        case 1: return launch_pdl(row_norm_kernel<1>, dim3(rows), dim3(256), 0, st, nm, x, x_stride, in, out);
+        case 2: return launch_pdl(row_norm_kernel<2>, dim3(rows), dim3(256), 0, st, nm, x, x_stride, in, out);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 int qlinear_rows_per_pass(int in) {
     // x of a pass, as fp32, within the shared-memory cap
@@ -268,6 +298,9 @@ int qlinear_rows_per_pass(int in) {
 
 cudaError_t launch_qlinear(const QLinearArgs& a, cudaStream_t st) {
     if (a.rows == 0) return cudaSuccess;
+    // many rows (a prefill): the tensor-core GEMM, which reads each weight
+    // once per 128 rows instead of once per pass of up to four
+    if (a.norm.kind == 0 && a.rows >= kQgemmMinRows) return launch_qgemm(a, st);
     int nb = qlinear_rows_per_pass(a.in);
     while (nb > 1 && nb / 2 >= a.rows) nb /= 2;  // no wider pass than the rows there are
     switch (nb) {

@@ -216,12 +216,18 @@ m2_status mamba2_gated_norm(const m2_dims* d, int rows, const void* y, const voi
  *   in_features/64] bf16. y: [rows, out_features] bf16; must not alias x.
  * Sizes: in_features a multiple of 64, at most 16384 (the Nemotron-H in_proj
  *   has 4480 -> 22656, out_proj 10240 -> 4480); rows >= 0 (rows == 0 is a
- *   no-op once the arguments check out). Each pass over the weights takes up
- *   to 4 rows of x (2 for in_features above 12480), so the weight traffic
- *   grows with rows: this form is for the few rows of a cached decode step.
+ *   no-op once the arguments check out).
+ * Forms: below 40 rows (the few rows of a cached decode step) each pass over
+ *   the weights takes up to 4 rows of x (2 for in_features above 12480);
+ *   from 40 rows (a prefill) the layer runs as a tensor-core GEMM over tiles
+ *   of 128 rows, the products of x with the exact bf16 (128 + q) per group
+ *   of 64 inputs accumulated in fp32 and scaled per group in fp32. Both give
+ *   the same sums in a different order (the results agree within rounding).
  * Errors: M2_EINVAL (NULL pointer, non-positive size), M2_EUNSUPPORTED
  *   (group_size other than 64 or bits other than 4, or not an sm_103 GPU),
- *   M2_ESHAPE (in_features), M2_EALIGN, M2_ECUDA. Asynchronous on `stream`. */
+ *   M2_ESHAPE (in_features), M2_EALIGN, M2_ECUDA. A bounded wait of the GEMM
+ *   that runs out records 0x101 (mamba2_device_error). Asynchronous on
+ *   `stream`. */
 m2_status mamba2_qlinear(int rows, int in_features, int out_features, int group_size, int bits, const void* x,
                          const uint32_t* wq, const void* scales, const void* biases, void* y, void* stream);
 
@@ -258,7 +264,10 @@ typedef struct {
  *     residual stream updated in place).
  * Errors as mamba2_qlinear, and M2_EINVAL / M2_ESHAPE / M2_EALIGN for a bad
  * norm. With x_stride = in_features and no norm or residual the results are
- * mamba2_qlinear's. */
+ * mamba2_qlinear's. The GEMM form (40 rows or more) is taken without a norm
+ * only: with one, every row count runs as passes of up to 4 rows (the
+ * library allocates no buffer for the normalised rows; mamba2_lm_prefill
+ * normalises into its workspace and then calls the GEMM). */
 m2_status mamba2_qlinear_fused(int rows, int in_features, int out_features, int group_size, int bits,
                                const void* x, long x_stride, const m2_row_norm* norm, const uint32_t* wq,
                                const void* scales, const void* biases, const void* residual, void* y,

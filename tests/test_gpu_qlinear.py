@@ -83,3 +83,61 @@ def test_qlinear_zero_rows_is_a_noop(m2):
     m2.mamba2_qlinear(0, 128, 16, x, wq, to_dev(inp["scales"]), to_dev(inp["biases"]), y)
     torch.cuda.synchronize()
     assert (y == 3.0).all()
+
+
+# ------------------------------------------------ many rows: the tensor-core GEMM
+# From 40 rows of x without a fused norm the layer runs as a tcgen05 GEMM over
+# tiles of 128 rows x 64 outputs, one 64-input group per accumulation.
+@pytest.mark.parametrize("rows,n_in,n_out", [
+    (40, 64, 136),        # the fewest rows and one group; 8 outputs past two tiles (enough
+                          # elements for the 0.1% share gate to allow a miss near zero)
+    (129, 128, 65),       # one row and one output past a tile
+    (200, 4480, 100),     # in_proj's input width
+    (300, 4480, 22656),   # in_proj over a 300-position prefill
+    (300, 10240, 4480),   # out_proj over a 300-position prefill
+])
+def test_qlinear_gemm_shapes(m2, rows, n_in, n_out):
+    inp = qlinear_inputs(rows * 7 + n_in + n_out, rows, n_in, n_out)
+    y = gpu_qlinear(m2, inp, rows, n_in, n_out)
+    assert m2.mamba2_device_error() == 0
+    check_y(from_dev_act(y, "bf16"), oracle_qlinear(inp), "bf16")
+
+
+def test_qlinear_gemm_worked_example(m2):
+    """The hand-written two-row weights of the worked example, read by 40 rows
+    of x (the GEMM): unit vectors at each of the 8 field positions of a word
+    and at both ends of the group pin the nibble order; every result is
+    exact in bf16."""
+    from seeded_inputs import f32_to_bf16_bits
+    wq = np.array([[0x76543210, 0xFEDCBA98] * 4, [0x89ABCDEF, 0x01234567] * 4], dtype=np.uint32)
+    cols = [13, 63, 0, 8, 1, 2, 3, 4, 5, 6, 7, 9, 33, 62, 31, 32, 47, 48, 15] * 2 + [40]
+    xs = np.zeros((len(cols) + 1, 64), dtype=np.float32)
+    xs[0] = 1.0
+    for r, i in enumerate(cols):
+        xs[r + 1, i] = 1.0
+    inp = dict(x=f32_to_bf16_bits(xs), wq=wq, scales=f32_to_bf16_bits(np.array([[0.5], [2.0]], np.float32)),
+               biases=f32_to_bf16_bits(np.array([[-4.0], [1.0]], np.float32)))
+    y = gpu_qlinear(m2, inp, xs.shape[0], 64, 2).float().cpu().numpy()
+    q0 = np.array([i % 16 for i in range(64)], np.float64)
+    q1 = 15 - q0
+    ref = np.stack([xs @ (0.5 * q0 - 4.0), xs @ (2.0 * q1 + 1.0)], axis=1)
+    np.testing.assert_array_equal(y, ref)
+
+
+def test_qlinear_gemm_residual_and_row_stride(m2):
+    """The GEMM with x read as a slice of wider rows and a residual added
+    before the one rounding (mamba2_qlinear_fused without a norm)."""
+    import torch
+    rows, n_in, n_out, pitch = 96, 256, 136, 320
+    inp = qlinear_inputs(4321, rows, n_in, n_out)
+    xw = torch.zeros((rows, pitch), dtype=torch.bfloat16, device="cuda")
+    xw[:, 32:32 + n_in] = to_dev(inp["x"])
+    res = torch.randn((rows, n_out), device="cuda").to(torch.bfloat16)
+    y = torch.full((rows, n_out), float("nan"), dtype=torch.bfloat16, device="cuda")
+    wq = torch.from_numpy(inp["wq"].view(np.int32)).cuda()
+    m2.mamba2_qlinear_fused(rows, n_in, n_out, xw[:, 32:], pitch, None, wq, to_dev(inp["scales"]),
+                            to_dev(inp["biases"]), res, y)
+    torch.cuda.synchronize()
+    assert m2.mamba2_device_error() == 0
+    ref = oracle_qlinear(inp) + from_dev_act(res, "bf16")
+    check_y(from_dev_act(y, "bf16"), ref, "bf16")
