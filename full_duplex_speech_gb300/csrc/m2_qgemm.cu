@@ -11,14 +11,13 @@
 //       threads into the same layout, plus one row of ones (so that the
 //       product also gives sum_i x_i over the group) and zero rows up to 80
 //   D_g = A B^T                 tcgen05.mma, fp32 in tensor memory (4 K-steps)
-// and, while the next group's products run, every thread takes its row of
-// D_g out of tensor memory and accumulates in fp32
+// and the epilogue warps take their rows of D_g out of tensor memory and
+// accumulate in fp32
 //   y += scale * D_g[o] + (bias - 128 scale) * D_g[ones]
 // which is the decode kernel's arithmetic (exact bf16 products, fp32 sums,
 // the group's scale and bias applied once per output), summed in a different
-// order. The x tiles run two groups ahead in three buffers, the weights'
-// fields and scales three groups ahead in registers; two buffers of B and D
-// alternate between groups.
+// order. Decode, products and epilogue run in warps of their own, on
+// different groups at once, through rings of three stages.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -32,23 +31,23 @@ namespace m2 {
 
 namespace {
 
-constexpr int kGmThreads = 256;
+constexpr int kGmThreads = 288;    // warps 0-3: epilogue (one TMEM lane quarter each); 4-7: decode; 8: copies and products
 constexpr int kGmRows = 128;       // rows of x per tile (the MMA's M, one per TMEM lane)
 constexpr int kGmOut = 64;         // outputs per tile
 constexpr int kGmN = 80;           // MMA N: 64 outputs, the ones row, 15 zero rows
 constexpr int kGroup = 64;         // inputs per quantization group (one K panel of 128 B)
+constexpr int kStages = 3;         // groups in flight: B tile, scales and accumulator of each
+constexpr int kAStages = 3;        // x tiles in flight (copies run kAStages - 2 groups ahead of the products)
 constexpr uint32_t kATile = kGmRows * 128;  // 16 KB
 constexpr uint32_t kBTile = kGmN * 128;     // 10 KB
-constexpr uint32_t kColD1 = 128;            // TMEM columns of the second D buffer
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 256;         // kStages accumulators of kGmN columns
 
-constexpr int kAStages = 3;  // x tiles in flight: groups g .. g + 2
 struct GmSmem {
-    static constexpr uint32_t kA = 0;                      // kAStages x A tile (1024-byte aligned)
-    static constexpr uint32_t kB = kAStages * kATile;      // 2 x B tile
-    static constexpr uint32_t kS = kB + 2 * kBTile;        // 2 x float2 (scale, bias - 128 scale) [64]
-    static constexpr uint32_t kBar = kS + 2 * kGmOut * 8;  // xbar[3], mbar[2], end
-    static constexpr uint32_t kTmem = kBar + 6 * 8;
+    static constexpr uint32_t kA = 0;                             // kAStages x A tile (1024-byte aligned)
+    static constexpr uint32_t kB = kAStages * kATile;             // kStages x B tile
+    static constexpr uint32_t kS = kB + kStages * kBTile;         // kStages x float2 (scale, bias - 128 scale) [64]
+    static constexpr uint32_t kBar = kS + kStages * kGmOut * 8;   // xfull [kAStages], bfull, dfull, empty [kStages], end
+    static constexpr uint32_t kTmem = kBar + (kAStages + 3 * kStages + 1) * 8;
     static constexpr uint32_t kFlag = kTmem + 4;
     // + slack to align the base to 1024; at least 80 KB, so that at most two
     // CTAs share an SM and their TMEM allocations (256 columns each) fit
@@ -63,23 +62,41 @@ __device__ __forceinline__ uint32_t nat_pair(uint32_t w, int j) {
     return lo | hi | 0x43004300u;
 }
 
+// Warp roles, handing groups over through rings of kStages buffers (stage
+// s = g mod kStages for group g):
+//   decode (warps 4-7): wait until the epilogue has released stage s, write
+//     group g's weights into B[s] and its scales into S[s], arrive on bfull[s];
+//   issue (warp 8, one thread): copy x of group g + kAStages - 2 into its A
+//     buffer once the products that last read it are done; once bfull[s]
+//     and the x tile of group g are complete, issue group g's four products into accumulator s
+//     and commit them to dfull[s];
+//   epilogue (warps 0-3, one row of the tile per thread): wait on dfull[s],
+//     add the group into its 64 fp32 accumulators, arrive on empty[s].
 template <bool RES>
 __global__ void __launch_bounds__(kGmThreads) qgemm_kernel(QLinearArgs a, const __grid_constant__ CUtensorMap tmx) {
     using L = GmSmem;
     extern __shared__ uint8_t gm_raw[];
     uint8_t* sm = gm_raw + ((1024u - (tc::smem_u32(gm_raw) & 1023u)) & 1023u);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int o0 = blockIdx.x * kGmOut, t0 = blockIdx.y * kGmRows;
     const int in = a.in, ngroups = in / kGroup;
     float2* sS = reinterpret_cast<float2*>(sm + L::kS);
-    uint64_t* xbar = reinterpret_cast<uint64_t*>(sm + L::kBar);  // x tile landed, by A buffer
-    uint64_t* mbar = xbar + kAStages;                             // products done, by D buffer
-    uint64_t* endbar = mbar + 2;                                  // every product done (abort path)
+    uint64_t* xfull = reinterpret_cast<uint64_t*>(sm + L::kBar);  // x tile landed
+    uint64_t* bfull = xfull + kAStages;                           // B tile and scales written (128 producers)
+    uint64_t* dfull = bfull + kStages;                            // products done
+    uint64_t* empty = dfull + kStages;                            // accumulator and scales read (128 epilogue threads)
+    uint64_t* endbar = empty + kStages;                           // every product done (abort path)
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::kTmem);
     volatile uint32_t* sFlag = reinterpret_cast<uint32_t*>(sm + L::kFlag);
 
     if (tid == 0) {
-        for (int i = 0; i < kAStages + 3; ++i) tc::mbar_init(xbar + i, 1);
+        for (int i = 0; i < kAStages; ++i) tc::mbar_init(xfull + i, 1);
+        for (int i = 0; i < kStages; ++i) {
+            tc::mbar_init(bfull + i, 128);
+            tc::mbar_init(dfull + i, 1);
+            tc::mbar_init(empty + i, 128);
+        }
+        tc::mbar_init(endbar, 1);
         tc::fence_mbar_init();
         *sFlag = 0;
     }
@@ -87,8 +104,8 @@ __global__ void __launch_bounds__(kGmThreads) qgemm_kernel(QLinearArgs a, const 
         tc::tmem_alloc(sTmem, kTmemCols);
         tc::tmem_relinquish();
     }
-    // the constant rows of both B tiles: the ones row (64) and zero rows 65..79
-    for (int e = tid; e < 2 * (kGmN - kGmOut) * 8; e += kGmThreads) {
+    // the constant rows of every B tile: the ones row (64) and zero rows 65..79
+    for (int e = tid; e < kStages * (kGmN - kGmOut) * 8; e += kGmThreads) {
         const int buf = e / ((kGmN - kGmOut) * 8), r = kGmOut + (e / 8) % (kGmN - kGmOut), c = e % 8;
         const uint32_t v = r == kGmOut ? 0x3F803F80u : 0u;  // bf16 1.0 pairs
         *reinterpret_cast<uint4*>(sm + L::kB + buf * kBTile + tc::sw128_off(r, c * 8, kGmN)) = make_uint4(v, v, v, v);
@@ -108,145 +125,159 @@ __global__ void __launch_bounds__(kGmThreads) qgemm_kernel(QLinearArgs a, const 
         return false;
     };
 
-    // decode work of this thread: weight row dr (0..63), inputs 16 dq .. 16 dq + 15 of a group
-    const int dr = tid >> 2, dq = tid & 3;
-    const bool drow_live = o0 + dr < a.out;
-    const uint2* wrow = reinterpret_cast<const uint2*>(a.wq + (size_t)(drow_live ? o0 + dr : 0) * (uint32_t)(in / 8));
-    // epilogue work: row 32 (warp % 4) + lane of the tile, outputs 32 (warp / 4) .. + 31
-    const int eq = warp & 3, eh = warp >> 2;
-    float acc[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-
     pdl_wait();  // x (and the residual) may come from the previous kernel
-    // x tile of group gx into its A buffer (thread 0); the buffer was last read
-    // by group gx - 3's products, complete before this is called
-    auto issue_x = [&](int gx) {
-        if (gx < ngroups && !*sFlag) {
-            uint64_t* bar = xbar + gx % kAStages;
-            tc::mbar_arrive_expect_tx(bar, kATile);
-            tc::tma_load_2d(sm + L::kA + (gx % kAStages) * kATile, &tmx, gx * kGroup, t0, bar);
-        }
-    };
-    if (tid == 0) {
-        issue_x(0);
-        issue_x(1);
-        issue_x(2);
-    }
-    // this thread's weight fields (and, for tid < 64, its output's scale and
-    // bias) of groups g, g + 1, g + 2, rotated each group
-    // (pinned loads: issued where they stand, three groups before their use)
-    auto load_w = [&](int gw) -> uint2 {
-        return (gw < ngroups && drow_live) ? ldg_pinned_u2(wrow + (size_t)gw * 4 + dq) : make_uint2(0u, 0u);
-    };
-    const bool srow_live = tid < kGmOut && o0 + tid < a.out;
-    const size_t srow = (size_t)(srow_live ? o0 + tid : 0) * ngroups;
-    auto load_s = [&](int gs) -> uint32_t {
-        return (gs < ngroups && srow_live)
-                   ? (uint32_t)ldg_pinned_u16(a.scales + srow + gs) | ((uint32_t)ldg_pinned_u16(a.biases + srow + gs) << 16)
-                   : 0u;
-    };
-    uint2 w0 = load_w(0), w1 = load_w(1), w2 = load_w(2);
-    uint32_t s0 = load_s(0), s1 = load_s(1), s2 = load_s(2);
-
-    const uint32_t sbase = tc::smem_u32(sm);
-    const uint32_t idesc = tc::idesc_bf16(kGmRows, kGmN, 0, 0);
-    for (int g = 0; g <= ngroups; ++g) {
-        const int p = g & 1;
-        if (g < ngroups && !*sFlag) {
-            // the weights of group g -> B[p] rows 0..63 (zeros past the last output);
-            // B[p] was last read by group g - 2's products, done (waited for in
-            // every thread's epilogue of that group)
-            const uint32_t ws[2] = {w0.x, w0.y};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint4 v;
-                v.x = nat_pair(ws[h], 0);
-                v.y = nat_pair(ws[h], 1);
-                v.z = nat_pair(ws[h], 2);
-                v.w = nat_pair(ws[h], 3);
-                if (!drow_live) v = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(sm + L::kB + p * kBTile + tc::sw128_off(dr, dq * 16 + h * 8, kGmN)) = v;
-            }
-            // the group's scale and bias - 128 scale of each output
-            if (tid < kGmOut) {
-                const float sc = bf16_bits_to_float(s0 & 0xFFFFu), bi = bf16_bits_to_float(s0 >> 16);
-                sS[p * kGmOut + tid] = make_float2(sc, bi - 128.f * sc);
-            }
-            tc::fence_proxy_async_smem();
-            w0 = w1;
-            w1 = w2;
-            w2 = load_w(g + 3);
-            s0 = s1;
-            s1 = s2;
-            s2 = load_s(g + 3);
-        }
-        tc::tc_fence_before();
-        __syncthreads();  // B[p], S[p] written; every epilogue of group g - 2 finished
-        tc::tc_fence_after();
-        if (g < ngroups && tid == 0 && !*sFlag) {
-            const int ab = g % kAStages;
-            if (wait_ok(xbar + ab, (g / kAStages) & 1)) {
+    if (warp == 8) {
+        // ============================================================ issue
+        if (tid == 256) {
+            constexpr int kLead = kAStages - 2;  // x of group g + kLead is copied before group g's products
+            auto issue_x = [&](int gx) {
+                uint64_t* bar = xfull + gx % kAStages;
+                tc::mbar_arrive_expect_tx(bar, kATile);
+                tc::tma_load_2d(sm + L::kA + (gx % kAStages) * kATile, &tmx, gx * kGroup, t0, bar);
+            };
+            for (int gx = 0; gx < kLead && gx < ngroups; ++gx) issue_x(gx);
+            const uint32_t sbase = tc::smem_u32(sm);
+            const uint32_t idesc = tc::idesc_bf16(kGmRows, kGmN, 0, 0);
+            for (int g = 0; g < ngroups; ++g) {
+                const int st = g % kStages;
+                const uint32_t rnd = (uint32_t)(g / kStages);
+                if (g + kLead < ngroups) {
+                    // A of group g + kLead last served group g - 2, whose products
+                    // were committed to dfull two groups ago
+                    if (g + kLead >= kAStages && !wait_ok(dfull + (g - 2) % kStages, (uint32_t)((g - 2) / kStages) & 1))
+                        break;
+                    issue_x(g + kLead);
+                }
+                const int ab = g % kAStages;
+                if (!wait_ok(bfull + st, rnd & 1) || !wait_ok(xfull + ab, (uint32_t)(g / kAStages) & 1)) break;
                 tc::tc_fence_after();
                 const uint64_t ad = tc::sdesc(sbase + L::kA + ab * kATile, 0, 1024, 2);
-                const uint64_t bd = tc::sdesc(sbase + L::kB + p * kBTile, 0, 1024, 2);
+                const uint64_t bd = tc::sdesc(sbase + L::kB + st * kBTile, 0, 1024, 2);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tm + (p ? kColD1 : 0u), ad + 2 * ks, bd + 2 * ks, idesc, ks > 0 ? 1u : 0u);
-                tc::mma_commit(mbar + p);
+                    tc::mma_bf16(tm + st * kGmN, ad + 2 * ks, bd + 2 * ks, idesc, ks > 0 ? 1u : 0u);
+                tc::mma_commit(dfull + st);
             }
         }
-        if (g > 0) {
-            // epilogue of group g - 1: D row -> fp32 accumulators
-            const int pp = (g - 1) & 1;
-            if (wait_ok(mbar + pp, ((g - 1) >> 1) & 1)) {
-                tc::tc_fence_after();
-                // group g - 1's products are done: its A buffer takes group g + 2
-                if (tid == 0) issue_x(g + 2);
-                const uint32_t ta = tm + ((uint32_t)(eq * 32) << 16) + (pp ? kColD1 : 0u);
-                float d0[16], d1[16], dx[8];
-                tc::tmem_ld16(ta + eh * 32, d0);
-                tc::tmem_ld16(ta + eh * 32 + 16, d1);
-                tc::tmem_ld8(ta + kGmOut, dx);  // column 64: sum of x over the group
+    } else if (warp >= 4) {
+        // ============================================================ decode
+        const int pt = tid - 128;
+        const int dr = pt >> 1, dh = pt & 1;  // weight row; inputs 32 dh .. 32 dh + 31 of a group
+        const bool drow_live = o0 + dr < a.out;
+        const uint4* wrow =
+            reinterpret_cast<const uint4*>(a.wq + (size_t)(drow_live ? o0 + dr : 0) * (uint32_t)(in / 8));
+        const bool srow_live = pt < kGmOut && o0 + pt < a.out;
+        const size_t srow = (size_t)(srow_live ? o0 + pt : 0) * ngroups;
+        // this thread's weight fields (and, for pt < 64, its output's scale and
+        // bias) of groups g .. g + kStages - 1: pinned loads, issued where they stand
+        auto load_w = [&](int gw) -> uint4 {
+            return (gw < ngroups && drow_live) ? ldg_pinned_u4(wrow + (size_t)gw * 2 + dh) : make_uint4(0u, 0u, 0u, 0u);
+        };
+        auto load_s = [&](int gs) -> uint32_t {
+            return (gs < ngroups && srow_live)
+                       ? (uint32_t)ldg_pinned_u16(a.scales + srow + gs) |
+                             ((uint32_t)ldg_pinned_u16(a.biases + srow + gs) << 16)
+                       : 0u;
+        };
+        // the ring is indexed by the stage, so the loop runs kStages groups per
+        // pass with every index fixed: a rotated ring would copy each load's
+        // register one group after issuing it, waiting for it there
+        uint4 wr[kStages];
+        uint32_t sr[kStages];
+#pragma unroll
+        for (int k = 0; k < kStages; ++k) {
+            wr[k] = load_w(k);
+            sr[k] = load_s(k);
+        }
+        bool stop = false;
+        for (int g0 = 0; g0 < ngroups && !stop; g0 += kStages) {
+#pragma unroll
+            for (int st = 0; st < kStages; ++st) {
+                const int g = g0 + st;
+                // stage st is free once the epilogue has finished group g - kStages
+                // (its accumulator and scales read, the products that read B[st] done)
+                if (g >= ngroups || stop ||
+                    (g0 > 0 && !wait_ok(empty + st, ((uint32_t)(g0 / kStages) - 1) & 1))) {
+                    stop = true;
+                    continue;
+                }
+                // the weights of group g -> B[st] rows 0..63 (zeros past the last output)
+                const uint32_t ws[4] = {wr[st].x, wr[st].y, wr[st].z, wr[st].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uint4 v;
+                    v.x = nat_pair(ws[k], 0);
+                    v.y = nat_pair(ws[k], 1);
+                    v.z = nat_pair(ws[k], 2);
+                    v.w = nat_pair(ws[k], 3);
+                    if (!drow_live) v = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(sm + L::kB + st * kBTile + tc::sw128_off(dr, dh * 32 + k * 8, kGmN)) = v;
+                }
+                if (pt < kGmOut) {
+                    const float sc = bf16_bits_to_float(sr[st] & 0xFFFFu), bi = bf16_bits_to_float(sr[st] >> 16);
+                    sS[st * kGmOut + pt] = make_float2(sc, bi - 128.f * sc);
+                }
+                wr[st] = load_w(g + kStages);
+                sr[st] = load_s(g + kStages);
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(bfull + st);
+            }
+        }
+    } else {
+        // ============================================================ epilogue
+        float acc[kGmOut];
+#pragma unroll
+        for (int j = 0; j < kGmOut; ++j) acc[j] = 0.f;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        for (int g = 0; g < ngroups; ++g) {
+            const int st = g % kStages;
+            // bfull orders the decode warps' scales before these reads
+            if (!wait_ok(bfull + st, (uint32_t)(g / kStages) & 1) || !wait_ok(dfull + st, (uint32_t)(g / kStages) & 1))
+                break;
+            tc::tc_fence_after();
+            const uint32_t ta = tm + lane_base + st * kGmN;
+            float dx[8];
+            tc::tmem_ld8(ta + kGmOut, dx);  // column 64: sum of x over the group
+            tc::tmem_wait_ld();
+            const float2* sc = sS + st * kGmOut;
+#pragma unroll
+            for (int q = 0; q < kGmOut / 16; ++q) {
+                float d[16];
+                tc::tmem_ld16(ta + q * 16, d);
                 tc::tmem_wait_ld();
-                const float2* sc = sS + pp * kGmOut + eh * 32;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float2 c0 = sc[j], c1 = sc[16 + j];
-                    acc[j] = fmaf(c0.x, d0[j], fmaf(c0.y, dx[0], acc[j]));
-                    acc[16 + j] = fmaf(c1.x, d1[j], fmaf(c1.y, dx[0], acc[16 + j]));
+                    const float2 c = sc[q * 16 + j];
+                    acc[q * 16 + j] = fmaf(c.x, d[j], fmaf(c.y, dx[0], acc[q * 16 + j]));
                 }
             }
             tc::tc_fence_before();
-            __syncthreads();  // S[pp] and D[pp] read by all before group g + 1 refills them
-            tc::tc_fence_after();
+            tc::mbar_arrive(empty + st);
         }
-    }
-
-    // the tile of y: row t, outputs o0 + 32 eh + j, plus the residual, rounded once
-    const int t = t0 + eq * 32 + lane;
-    if (!*sFlag && t < a.rows) {
-        const int ob = o0 + eh * 32;
-        uint16_t* yrow = reinterpret_cast<uint16_t*>(a.y) + (size_t)t * a.out;
-        const uint16_t* rrow = reinterpret_cast<const uint16_t*>(a.residual) + (size_t)t * a.out;
+        // the tile of y: row t, outputs o0 .. o0 + 63, plus the residual, rounded once
+        const int t = t0 + tid;
+        if (!*sFlag && t < a.rows) {
+            uint16_t* yrow = reinterpret_cast<uint16_t*>(a.y) + (size_t)t * a.out;
+            const uint16_t* rrow = reinterpret_cast<const uint16_t*>(a.residual) + (size_t)t * a.out;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (ob + j < a.out) {
-                const float res = RES ? bf16_bits_to_float(rrow[ob + j]) : 0.f;
-                yrow[ob + j] = float_to_bf16_bits(acc[j] + res);
+            for (int j = 0; j < kGmOut; ++j) {
+                if (o0 + j < a.out) {
+                    const float res = RES ? bf16_bits_to_float(rrow[o0 + j]) : 0.f;
+                    yrow[o0 + j] = float_to_bf16_bits(acc[j] + res);
+                }
             }
         }
     }
     pdl_trigger();
-    if (*sFlag && tid == 0) {
+    if (*sFlag && tid == 256) {
         // A wait gave up. Every product issued must be done, and the x copies
         // in flight must land, before the tensor memory is freed and the CTA
         // exits (all waits bounded).
         tc::mma_commit(endbar);
         tc::mbar_wait(endbar, 0, 100000000ull);
         for (int i = 0; i < kAStages; ++i) {
-            tc::mbar_wait(xbar + i, 0, 100000000ull);
-            tc::mbar_wait(xbar + i, 1, 100000000ull);
+            tc::mbar_wait(xfull + i, 0, 100000000ull);
+            tc::mbar_wait(xfull + i, 1, 100000000ull);
         }
     }
     tc::tc_fence_before();
