@@ -33,11 +33,6 @@ __device__ __forceinline__ uint4 ldg_pinned_u4(const void* p) {
                  : "memory");
     return r;
 }
-__device__ __forceinline__ uint2 ldg_pinned_u2(const void* p) {
-    uint2 r;
-    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p) : "memory");
-    return r;
-}
 __device__ __forceinline__ float4 ldg_pinned_f4(const void* p) {
     float4 r;
     asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
