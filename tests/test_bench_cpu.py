@@ -79,3 +79,23 @@ def test_lm_position_unit_count():
             + 750 * 8 * 128 * 2 * 2 + 8 * 128 * 2 * 2)            # cached keys and values read, new ones written
     residual = 31 * 4480 * 2 * 2
     assert b.lm_position_bytes(REAL_LM, 1, 750) == 27 * mamba + 4 * attn + residual == 2978602496
+
+
+def test_reference_arm_under_two_ranks():
+    """Launched as the driver launches it for N > 1 (torchrun, one process per
+    rank; gloo on a host without GPUs): rank 0 alone runs the oracle and
+    prints the one JSON line, the other rank exits 0 without work."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.lstrip().startswith("{")]
+    assert len(lines) == 1, r.stdout[-3000:]
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
