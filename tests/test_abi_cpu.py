@@ -38,6 +38,13 @@ def test_library_exports_every_declared_symbol(m2):
         assert hasattr(lib, n), n
 
 
+def test_binding_has_every_declared_function(m2):
+    """The Python binding carries the header's names one for one."""
+    missing = [n for n in _declared_functions() if not callable(getattr(m2, n, None))]
+    assert not missing, missing
+    assert all(n in m2.__all__ for n in _declared_functions())
+
+
 def test_status_strings(m2):
     for s in range(7):
         assert m2.mamba2_status_string(s)
