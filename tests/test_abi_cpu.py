@@ -412,3 +412,18 @@ def test_lm_workspace_plan(m2):
         assert floor <= got <= floor + 16 * 256, (T, got, floor)
     # from 40 rows the normalised rows are part of it
     assert m2.mamba2_lm_workspace_bytes(m, 1, 40, 128) - m2.mamba2_lm_workspace_bytes(m, 1, 39, 128) >= 40 * HP * 2
+
+
+@pytest.mark.skipif(not NO_GPU, reason="host tensors would reach a launch where a GPU is present")
+def test_readme_example_passes_the_host_checks(m2):
+    """The README's Python example, run on host tensors: every call gets past
+    all of its argument checks and stops only at the device check."""
+    src = open(os.path.join(ROOT, "README.md")).read()
+    code = re.search(r"```python\n(.*?)```", src, re.S).group(1)
+    code = code.replace('dev, bf = "cuda", torch.bfloat16', 'dev, bf = "cpu", torch.bfloat16')
+    code = code.split("torch.cuda.synchronize()")[0]
+    code = re.sub(r"^(m2\.mamba2_\w+\()", r"_rc.append(\1", code, flags=re.M)
+    code = re.sub(r"(ws|wss)\)\n", r"\1, stream=0, check=False))\n", code)
+    rcs = []
+    exec(compile(code, "README.md", "exec"), {"_rc": rcs})
+    assert len(rcs) == 2 and all(rc == 5 for rc in rcs), rcs   # M2_ECUDA: no device here
