@@ -68,8 +68,8 @@ __device__ __forceinline__ uint32_t nat_pair(uint32_t w, int j) {
 //     group g's weights into B[s] and its scales into S[s], arrive on bfull[s];
 //   issue (warp 8, one thread): copy x of group g + kAStages - 2 into its A
 //     buffer once the products that last read it are done; once bfull[s]
-//     and the x tile of group g are complete, issue group g's four products into accumulator s
-//     and commit them to dfull[s];
+//     and the x tile of group g are complete, issue group g's four products
+//     into accumulator s and commit them to dfull[s];
 //   epilogue (warps 0-3, one row of the tile per thread): wait on dfull[s],
 //     add the group into its 64 fp32 accumulators, arrive on empty[s].
 template <bool RES>
